@@ -1,0 +1,105 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module only draws random numbers and lays them out; it holds none of the
+attention arithmetic, so the CUDA path and the CPU oracle can both take their
+inputs from it without sharing any of the method.
+
+Every workload is (B, H, N, d) bf16 Q, K, V drawn i.i.d. N(0, 1) from
+``torch.Generator('cpu').manual_seed(seed)`` in the order Q, K, V (fp32, then
+rounded to bf16).  The rescale-stress workload also multiplies Q by 4 and
+every 512th key row (0-based index j with j % 512 == 511) by 8; both factors
+are powers of two, so they commute with the rounding to bf16.
+
+The shapes follow the pages' running example ("Kernels — fusion and
+FlashAttention" §2: B = 8, h = 32 heads, bf16, where a naive score matrix
+takes 8.6 GB at T = 4096) and head sizes d in {64, 128} ("Writing and
+Benchmarking Custom Kernels" §10.3.1 worked example: d_head = 128, 32 heads).
+No public dataset is involved.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    q_mult: float = 1.0
+    spike_every: int = 0       # every spike_every-th key row is multiplied ...
+    spike_mult: float = 1.0    # ... by spike_mult
+    sample_rows: int = 0       # rows compared with the oracle; 0 = the full tensor
+
+    @property
+    def shape(self):
+        return (self.B, self.H, self.N, self.d)
+
+    @property
+    def scale(self) -> float:
+        """1/sqrt(d) rounded to fp32, the value both sides are given."""
+        return float(np.float32(1.0 / np.sqrt(self.d)))
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("b1_h2_n256_d64", 1, 2, 256, 64, False, 1001),
+        Workload("b4_h16_n2048_d128_causal", 4, 16, 2048, 128, True, 1002),
+        Workload("b8_h32_n4096_d128_causal", 8, 32, 4096, 128, True, 1003, sample_rows=512),
+        Workload("b1_h32_n32768_d128_causal", 1, 32, 32768, 128, True, 1004, sample_rows=256),
+        Workload("b16_h16_n8192_d64_spiky", 16, 16, 8192, 64, False, 1005, q_mult=4.0,
+                 spike_every=512, spike_mult=8.0, sample_rows=512),
+    )
+}
+
+# The workload the throughput line is quoted on: the pages' B = 8, h = 32
+# example at T = 4096, d_head = 128, causal.
+HEADLINE = "b8_h32_n4096_d128_causal"
+
+
+def make_qkv(w: Workload, device="cpu"):
+    """Seeded bf16 (Q, K, V) of shape (B, H, N, d), generated on the CPU."""
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    q = torch.randn(w.shape, generator=g, dtype=torch.float32)
+    k = torch.randn(w.shape, generator=g, dtype=torch.float32)
+    v = torch.randn(w.shape, generator=g, dtype=torch.float32)
+    if w.q_mult != 1.0:
+        q.mul_(w.q_mult)
+    if w.spike_every:
+        k[:, :, w.spike_every - 1 :: w.spike_every, :] *= w.spike_mult
+    out = [t.to(torch.bfloat16) for t in (q, k, v)]
+    del q, k, v
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return tuple(out)
+
+
+def make_random_qkv(B, H, N, d, seed, q_mult=1.0, device="cpu"):
+    """Seeded i.i.d. N(0,1) bf16 tensors of an arbitrary shape (test cases)."""
+    return make_qkv(Workload("adhoc", B, H, N, d, False, seed, q_mult=q_mult), device)
+
+
+def sample_rows(w: Workload, n: int | None = None):
+    """Seeded (bh, row) pairs to compare with the oracle.
+
+    Always holds the first row of the first head and the last row of the last
+    head; the rest are drawn with ``numpy.random.default_rng(seed + 1)``.
+    Returns two int64 arrays (bh index = b*H + h, query row).
+    """
+    n = w.sample_rows if n is None else n
+    rng = np.random.default_rng(w.seed + 1)
+    bh = rng.integers(0, w.B * w.H, size=n, dtype=np.int64)
+    row = rng.integers(0, w.N, size=n, dtype=np.int64)
+    if n >= 1:
+        bh[0], row[0] = 0, 0
+    if n >= 2:
+        bh[1], row[1] = w.B * w.H - 1, w.N - 1
+    return bh, row

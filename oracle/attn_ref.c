@@ -1,0 +1,243 @@
+/*
+ * Oracle for softmax attention, fp64, plain C.  TEST INFRASTRUCTURE ONLY:
+ * nothing in the product path may link, load or call this file.
+ *
+ * What it computes, per (batch b, head h), for query row i:
+ *
+ *     s_ij = scale * sum_c q_ic k_jc                       (score row, fully materialised)
+ *     s_ij = -inf                      if causal and j > i (query i sees keys 0..i)
+ *     m_i  = max_j s_ij
+ *     e_ij = exp(s_ij - m_i),  l_i = sum_j e_ij,  P_ij = e_ij / l_i
+ *     O_ic = sum_j P_ij v_jc
+ *     L_i  = m_i + ln l_i                                   (logsumexp, natural log)
+ *
+ * Sources:
+ *   - "Kernels — fusion and FlashAttention" (jiahuanglin.xyz cs336 lesson 07),
+ *     §2 "Naive attention": scores, mask, softmax, weight the values; the
+ *     tensors are (B, h, T, d_head).
+ *   - same page, §3: softmax subtracts the row max for stability before
+ *     exponentiating and divides by the row sum.
+ *   - same page, §5: the forward saves m + log(l) per row (logsumexp).
+ *   - "Writing and Benchmarking Custom Kernels" (arunshar.com, ch. 10),
+ *     §10.3.1: S = QK^T / sqrt(d), m_i = max_j S_ij, denominator
+ *     sum_j exp(S_ij - m_i); §10.3.2: L_i = m_i + log l_i kept in fp32 by
+ *     the kernel (the oracle keeps fp64).
+ *   - same chapter, §10.3.1 "What you actually decide": causal masking drops
+ *     the key tiles above the diagonal.
+ *
+ * A second routine, oracle_attn_online_f64, carries out the tile-by-tile
+ * online-softmax recurrence of "Kernels — fusion and FlashAttention" §3 (running
+ * max m, running denominator l, running output o, each rescaled by
+ * exp(m_old - m_new) when a tile raises the max; out = o / l), in fp64, so that
+ * tests can check that the recurrence reaches the two-pass result.
+ *
+ * Inputs are bf16 bit patterns (uint16), widened exactly to fp64.  Layout is
+ * contiguous (B, H, N, d) row-major for q, k, v and o; (B, H, N) for lse.
+ * Nothing here is blocked, fused or reordered beyond the definition: the only
+ * parallelism is independent query rows spread over OpenMP threads.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_bits_to_f64(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* One query row i of one (b, h): materialise the score row, mask, two-pass
+ * softmax, P.V and the logsumexp.  s_row is caller-provided scratch of N
+ * doubles.  p_row (nullable) receives the probability row. */
+static void attention_row(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          int64_t N, int64_t d, int causal, double scale, int64_t i,
+                          double *s_row, double *o_row, double *lse, double *p_row)
+{
+    /* scores */
+    for (int64_t j = 0; j < N; ++j) {
+        if (causal && j > i) {
+            s_row[j] = -INFINITY;
+            continue;
+        }
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += bf16_bits_to_f64(q[i * d + c]) * bf16_bits_to_f64(k[j * d + c]);
+        s_row[j] = scale * acc;
+    }
+    /* pass 1: row max */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j)
+        if (s_row[j] > m) m = s_row[j];
+    /* pass 2: exponentials and their sum */
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        s_row[j] = exp(s_row[j] - m); /* exp(-inf) = 0 for masked keys */
+        l += s_row[j];
+    }
+    /* normalise, then weight the values */
+    for (int64_t j = 0; j < N; ++j) s_row[j] /= l;
+    if (p_row)
+        for (int64_t j = 0; j < N; ++j) p_row[j] = s_row[j];
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        const double p = s_row[j];
+        if (p == 0.0) continue;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_bits_to_f64(v[j * d + c]);
+    }
+    *lse = m + log(l);
+}
+
+static int bad_shape(int64_t B, int64_t H, int64_t N, int64_t d)
+{
+    return B < 1 || H < 1 || N < 1 || d < 1;
+}
+
+static int pick_threads(int nthreads)
+{
+#ifdef _OPENMP
+    return nthreads > 0 ? nthreads : omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* Full tensor.  o: B*H*N*d doubles, lse: B*H*N doubles, p (nullable):
+ * B*H*N*N doubles.  Returns 0 on success, -1 on bad arguments, -2 on
+ * allocation failure. */
+int oracle_attn_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                    int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                    double *o, double *lse, double *p, int nthreads)
+{
+    if (!q || !k || !v || !o || !lse || bad_shape(B, H, N, d)) return -1;
+    const int64_t rows = B * H * N;
+    int failed = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads))
+    {
+        double *s_row = (double *)malloc((size_t)N * sizeof(double));
+        if (!s_row) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!s_row) continue;
+            const int64_t bh = r / N, i = r % N;
+            const int64_t head = bh * N * d;
+            attention_row(q + head, k + head, v + head, N, d, causal, scale, i, s_row,
+                          o + r * d, lse + r, p ? p + r * N : NULL);
+        }
+        free(s_row);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Selected rows only: row t is query row_idx[t] of flattened head bh_idx[t]
+ * (bh = b*H + h).  o_rows: nrows*d, lse_rows: nrows. */
+int oracle_attn_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                         const int64_t *bh_idx, const int64_t *row_idx, int64_t nrows,
+                         double *o_rows, double *lse_rows, int nthreads)
+{
+    if (!q || !k || !v || !bh_idx || !row_idx || !o_rows || !lse_rows || nrows < 0 ||
+        bad_shape(B, H, N, d))
+        return -1;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (bh_idx[t] < 0 || bh_idx[t] >= B * H || row_idx[t] < 0 || row_idx[t] >= N) return -1;
+    int failed = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads))
+    {
+        double *s_row = (double *)malloc((size_t)N * sizeof(double));
+        if (!s_row) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < nrows; ++t) {
+            if (!s_row) continue;
+            const int64_t head = bh_idx[t] * N * d;
+            attention_row(q + head, k + head, v + head, N, d, causal, scale, row_idx[t], s_row,
+                          o_rows + t * d, lse_rows + t, NULL);
+        }
+        free(s_row);
+    }
+    return failed ? -2 : 0;
+}
+
+/* The online-softmax recurrence, keys taken `tile` at a time.  For each query
+ * row: m = -inf, l = 0, o = 0; for each key tile: scores s of the tile (masked
+ * keys at -inf), m_new = max(m, max s), c = exp(m - m_new),
+ * p = exp(s - m_new), l = l*c + sum p, o = o*c + p.V_tile, m = m_new; finally
+ * out = o / l and lse = m + ln l.  Under the causal mask a tile whose every
+ * key lies above the diagonal is skipped (it adds nothing). */
+int oracle_attn_online_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                           int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                           int64_t tile, double *o, double *lse, int nthreads)
+{
+    if (!q || !k || !v || !o || !lse || tile < 1 || bad_shape(B, H, N, d)) return -1;
+    const int64_t rows = B * H * N;
+    int failed = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads))
+    {
+        double *s = (double *)malloc((size_t)tile * sizeof(double));
+        double *acc = (double *)malloc((size_t)d * sizeof(double));
+        if (!s || !acc) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!s || !acc) continue;
+            const int64_t bh = r / N, i = r % N;
+            const uint16_t *qh = q + bh * N * d, *kh = k + bh * N * d, *vh = v + bh * N * d;
+            double m = -INFINITY, l = 0.0;
+            for (int64_t c = 0; c < d; ++c) acc[c] = 0.0;
+            for (int64_t j0 = 0; j0 < N; j0 += tile) {
+                if (causal && j0 > i) break; /* tile entirely above the diagonal */
+                const int64_t n = (j0 + tile <= N) ? tile : N - j0;
+                double tile_max = -INFINITY;
+                for (int64_t t = 0; t < n; ++t) {
+                    const int64_t j = j0 + t;
+                    if (causal && j > i) {
+                        s[t] = -INFINITY;
+                        continue;
+                    }
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += bf16_bits_to_f64(qh[i * d + c]) * bf16_bits_to_f64(kh[j * d + c]);
+                    s[t] = scale * dot;
+                    if (s[t] > tile_max) tile_max = s[t];
+                }
+                const double m_new = (tile_max > m) ? tile_max : m;
+                const double corr = exp(m - m_new); /* exp(-inf) = 0 on the first tile */
+                double psum = 0.0;
+                for (int64_t c = 0; c < d; ++c) acc[c] *= corr;
+                for (int64_t t = 0; t < n; ++t) {
+                    const double p = exp(s[t] - m_new);
+                    psum += p;
+                    if (p == 0.0) continue;
+                    const int64_t j = j0 + t;
+                    for (int64_t c = 0; c < d; ++c) acc[c] += p * bf16_bits_to_f64(vh[j * d + c]);
+                }
+                l = l * corr + psum;
+                m = m_new;
+            }
+            for (int64_t c = 0; c < d; ++c) o[r * d + c] = acc[c] / l;
+            lse[r] = m + log(l);
+        }
+        free(s);
+        free(acc);
+    }
+    return failed ? -2 : 0;
+}
+
+int oracle_max_threads(void)
+{
+    return pick_threads(0);
+}

@@ -1,0 +1,279 @@
+"""Pins for the CPU oracle, checked against things other than itself.
+
+Each pin is a plain function taking an oracle instance, so that the same
+battery can be run against copies of the oracle with a planted mistake
+(``test_planted_mistakes_are_caught``): every plausible slip -- a mask off by
+one, a transposed operand, a dropped scale or normalisation, a wrong sign, a
+wrong logarithm base, a missing rescale in the recurrence -- must fail at
+least one pin.
+
+What pins what (the statements are those of "Kernels — fusion and
+FlashAttention" §2–§3, "Fusion and IO-aware kernels" § FlashAttention, and
+"Writing and Benchmarking Custom Kernels" §10.3):
+  * library softmax / logsumexp (scipy) on tiny inputs -- the whole definition;
+  * exact closed forms: one key (O = V, L = scale·q·k), equal scores (O = mean
+    of the visible values, L = ln n), two keys (logistic weights);
+  * invariants: probability rows sum to one, constant values pass through,
+    a per-row score shift leaves O alone and moves L by the shift, key
+    permutation leaves non-causal rows alone, a causal row equals the
+    unmasked problem on its prefix, huge scores do not overflow;
+  * the tile-by-tile online recurrence reaches the two-pass result for every
+    tile size, including 1, sizes that do not divide N, and sizes above N.
+"""
+import math
+import os
+import re
+import shutil
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from io_aware_attention_gb300.workloads import make_random_qkv
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def f64(x):
+    return oracle.bf16_to_f64(x)
+
+
+def bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+# --------------------------------------------------------------------------- pins
+
+
+def pin_library_softmax(orc):
+    """scipy softmax / logsumexp of the masked, scaled score matrix."""
+    for (B, H, N, d, causal, seed) in [(1, 1, 1, 8, False, 1), (1, 2, 5, 8, True, 2),
+                                        (2, 1, 17, 64, False, 3), (1, 1, 17, 64, True, 4),
+                                        (1, 1, 9, 1, True, 5)]:
+        q, k, v = make_random_qkv(B, H, N, d, seed)
+        scale = 0.37
+        o, lse = orc.attention(q, k, v, causal, scale)
+        Q, K, V = f64(q), f64(k), f64(v)
+        S = scale * np.einsum("bhid,bhjd->bhij", Q, K)
+        if causal:
+            S = np.where(np.triu(np.ones((N, N), bool), 1), -np.inf, S)
+        P = scipy.special.softmax(S, axis=-1)
+        np.testing.assert_allclose(o, P @ V, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, scipy.special.logsumexp(S, axis=-1), rtol=1e-13,
+                                   atol=1e-13)
+
+
+def pin_single_key(orc):
+    """N = 1: the one key gets all the weight; L = scale·q·k exactly."""
+    q, k, v = make_random_qkv(2, 3, 1, 64, 11)
+    scale = 0.125
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, scale)
+        np.testing.assert_array_equal(o, f64(v))
+        Q, K = f64(q), f64(k)
+        for b in range(2):
+            for h in range(3):
+                exact = Fraction(scale) * sum(Fraction(float(a)) * Fraction(float(c))
+                                              for a, c in zip(Q[b, h, 0], K[b, h, 0]))
+                assert abs(lse[b, h, 0] - float(exact)) <= 1e-13 * max(1.0, abs(float(exact)))
+
+
+def pin_equal_scores(orc):
+    """Q = 0: all visible scores are 0, O = mean of the visible values, L = ln n."""
+    _, k, v = make_random_qkv(1, 2, 13, 16, 12)
+    q = torch.zeros_like(k)
+    V = f64(v)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.5)
+        for i in range(13):
+            n = i + 1 if causal else 13
+            mean = np.array([[float(sum(Fraction(float(x)) for x in V[0, h, :n, c]) / n)
+                              for c in range(16)] for h in range(2)])
+            np.testing.assert_allclose(o[0, :, i], mean, rtol=1e-14, atol=1e-15)
+            np.testing.assert_allclose(lse[0, :, i], math.log(n), rtol=1e-15, atol=1e-15)
+
+
+def pin_two_keys(orc):
+    """N = 2: weights are the logistic function of the score gap."""
+    q, k, v = make_random_qkv(1, 1, 2, 8, 13, q_mult=2.0)
+    scale = 0.3
+    Q, K, V = f64(q)[0, 0], f64(k)[0, 0], f64(v)[0, 0]
+    o, lse = orc.attention(q, k, v, False, scale)
+    oc, lsec = orc.attention(q, k, v, True, scale)
+    for i in range(2):
+        s0, s1 = scale * float(Q[i] @ K[0]), scale * float(Q[i] @ K[1])
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        np.testing.assert_allclose(o[0, 0, i], w0 * V[0] + (1.0 - w0) * V[1], rtol=1e-13,
+                                   atol=1e-14)
+        hi = max(s0, s1)
+        assert abs(lse[0, 0, i] - (hi + math.log1p(math.exp(-abs(s0 - s1))))) < 1e-13
+    # causal: row 0 sees key 0 only, row 1 sees both
+    np.testing.assert_array_equal(oc[0, 0, 0], V[0])
+    assert abs(lsec[0, 0, 0] - scale * float(Q[0] @ K[0])) < 1e-13
+    np.testing.assert_allclose(oc[0, 0, 1], o[0, 0, 1], rtol=1e-15, atol=1e-15)
+
+
+def pin_probability_rows(orc):
+    """P >= 0, rows sum to 1, and the causal mask zeroes exactly j > i."""
+    q, k, v = make_random_qkv(1, 2, 23, 32, 14)
+    for causal in (False, True):
+        _, _, p = orc.attention(q, k, v, causal, 0.2, return_probs=True)
+        assert (p >= 0).all()
+        np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-14)
+        upper = np.triu(np.ones((23, 23), bool), 1)
+        if causal:
+            assert (p[..., upper] == 0).all()
+            assert (p[..., ~upper] > 0).all()
+        else:
+            assert (p > 0).all()
+
+
+def pin_constant_values(orc):
+    """Every value row equal to c: O = c whatever the weights."""
+    q, k, _ = make_random_qkv(1, 2, 31, 64, 15)
+    c = make_random_qkv(1, 2, 1, 64, 16)[2]
+    v = c.expand(1, 2, 31, 64).contiguous()
+    for causal in (False, True):
+        o, _ = orc.attention(q, k, v, causal, 0.125)
+        np.testing.assert_allclose(o, np.broadcast_to(f64(c), o.shape), rtol=1e-14, atol=1e-15)
+
+
+def pin_score_shift(orc):
+    """Adding u to every key row shifts row i's scores by scale·q_i·u: O stays,
+    L moves by exactly that shift (integer-valued data keeps K + u exact)."""
+    rng = np.random.default_rng(17)
+    N, d, scale = 12, 8, 0.25
+    Qi = rng.integers(-3, 4, size=(1, 1, N, d))
+    Ki = rng.integers(-4, 5, size=(1, 1, N, d))
+    u = rng.integers(-2, 3, size=(d,))
+    Vv = rng.standard_normal((1, 1, N, d))
+    q, k, k2, v = bf16(Qi), bf16(Ki), bf16(Ki + u), bf16(Vv)
+    for causal in (False, True):
+        o1, l1 = orc.attention(q, k, v, causal, scale)
+        o2, l2 = orc.attention(q, k2, v, causal, scale)
+        np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-14)
+        np.testing.assert_allclose(l2 - l1, scale * (Qi @ u), rtol=0, atol=1e-12)
+
+
+def pin_key_permutation(orc):
+    """Non-causal rows do not depend on the order of the (key, value) pairs."""
+    q, k, v = make_random_qkv(1, 1, 19, 16, 18)
+    perm = torch.from_numpy(np.random.default_rng(19).permutation(19))
+    o1, l1 = orc.attention(q, k, v, False, 0.25)
+    o2, l2 = orc.attention(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), False, 0.25)
+    np.testing.assert_allclose(o2, o1, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(l2, l1, rtol=1e-14, atol=1e-14)
+
+
+def pin_causal_prefix(orc):
+    """Causal row i equals the unmasked problem on keys 0..i (last row there)."""
+    q, k, v = make_random_qkv(1, 1, 9, 16, 20)
+    oc, lc = orc.attention(q, k, v, True, 0.25)
+    for i in range(9):
+        sl = slice(0, i + 1)
+        o, l = orc.attention(q[:, :, sl].contiguous(), k[:, :, sl].contiguous(),
+                             v[:, :, sl].contiguous(), False, 0.25)
+        np.testing.assert_allclose(oc[0, 0, i], o[0, 0, i], rtol=1e-14, atol=1e-15)
+        assert abs(lc[0, 0, i] - l[0, 0, i]) < 1e-13
+
+
+def pin_huge_scores(orc):
+    """Scores in the thousands: with the max subtracted nothing overflows; the
+    row collapses onto the best key and L is the largest score."""
+    q, k, v = make_random_qkv(1, 1, 16, 64, 21, q_mult=64.0)
+    k = k * 8
+    o, lse = orc.attention(q, k, v, False, 1.0)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    S = f64(q)[0, 0] @ f64(k)[0, 0].T
+    assert S.max() > 1000.0
+    best = S.argmax(-1)
+    top2 = np.sort(S, -1)[:, -2:]
+    assert (top2[:, 1] - top2[:, 0] > 40).all()  # the runner-up weighs < e^-40
+    np.testing.assert_allclose(o[0, 0], f64(v)[0, 0][best], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], S.max(-1), rtol=1e-15, atol=1e-12)
+
+
+def pin_rows_entry(orc):
+    """Selected rows equal the same rows of the full computation."""
+    q, k, v = make_random_qkv(2, 3, 37, 16, 22)
+    bh = np.array([0, 5, 3, 2, 4, 1], np.int64)
+    row = np.array([0, 36, 17, 1, 35, 20], np.int64)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.3)
+        orow, lrow = orc.attention_rows(q, k, v, causal, 0.3, bh, row)
+        np.testing.assert_array_equal(orow, o.reshape(6, 37, 16)[bh, row])
+        np.testing.assert_array_equal(lrow, lse.reshape(6, 37)[bh, row])
+
+
+def pin_online_recurrence(orc):
+    """The tile-by-tile recurrence reaches the two-pass result for any tile size."""
+    q, k, v = make_random_qkv(1, 2, 100, 32, 23, q_mult=3.0)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.4)
+        for tile in (1, 3, 16, 64, 100, 105):
+            o2, l2 = orc.attention_online(q, k, v, causal, 0.4, tile)
+            np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(l2, lse, rtol=1e-13, atol=1e-12)
+
+
+PINS = [pin_library_softmax, pin_single_key, pin_equal_scores, pin_two_keys,
+        pin_probability_rows, pin_constant_values, pin_score_shift, pin_key_permutation,
+        pin_causal_prefix, pin_huge_scores, pin_rows_entry, pin_online_recurrence]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin(oracle)
+
+
+# --------------------------------------------------------- planted mistakes
+
+# (description, text to replace, replacement) -- each applied alone to a copy
+# of attn_ref.c.  Indexes stay in bounds so a mutant cannot crash the test.
+MUTANTS = [
+    ("mask off by one (diagonal hidden)", "if (causal && j > i) {\n            s_row[j]",
+     "if (causal && j >= i) {\n            s_row[j]"),
+    ("mask the wrong triangle", "if (causal && j > i) {\n            s_row[j]",
+     "if (causal && j < i) {\n            s_row[j]"),
+    ("transposed score operands", "q[i * d + c]) * bf16_bits_to_f64(k[j * d + c])",
+     "q[j * d + c]) * bf16_bits_to_f64(k[i * d + c])"),
+    ("scale dropped", "s_row[j] = scale * acc;", "s_row[j] = acc;"),
+    ("exp sign flipped", "s_row[j] = exp(s_row[j] - m);", "s_row[j] = exp(m - s_row[j]);"),
+    ("no normalisation", "for (int64_t j = 0; j < N; ++j) s_row[j] /= l;", ""),
+    ("values of the query row", "o_row[c] += p * bf16_bits_to_f64(v[j * d + c])",
+     "o_row[c] += p * bf16_bits_to_f64(v[i * d + c])"),
+    ("lse in base 2", "*lse = m + log(l);", "*lse = m + log2(l);"),
+    ("lse without the max", "*lse = m + log(l);", "*lse = log(l);"),
+    ("max not subtracted", "double m = -INFINITY;\n    for (int64_t j = 0; j < N; ++j)\n        if",
+     "double m = 0.0;\n    for (int64_t j = 0; j < N; ++j)\n        if (0) if"),
+    ("recurrence: output not rescaled", "for (int64_t c = 0; c < d; ++c) acc[c] *= corr;", ""),
+    ("recurrence: denominator not rescaled", "l = l * corr + psum;", "l = l + psum;"),
+    ("recurrence: causal tile skip off by one", "if (causal && j0 > i) break;",
+     "if (causal && j0 >= i) break;"),
+]
+
+
+def test_planted_mistakes_are_caught(tmp_path):
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")).read()
+    # the unmodified source, compiled the same way, passes every pin
+    clean = tmp_path / "clean.c"
+    clean.write_text(src)
+    orc = oracle.from_source(str(clean), str(tmp_path / "clean.so"))
+    for pin in PINS:
+        pin(orc)
+    for n, (what, old, new) in enumerate(MUTANTS):
+        assert src.count(old) == 1, f"mutation site not unique/found: {what}"
+        path = tmp_path / f"m{n}.c"
+        path.write_text(src.replace(old, new))
+        mut = oracle.from_source(str(path), str(tmp_path / f"m{n}.so"))
+        caught = []
+        with np.errstate(all="ignore"):
+            for pin in PINS:
+                try:
+                    pin(mut)
+                except (AssertionError, RuntimeError, FloatingPointError, ValueError):
+                    caught.append(pin.__name__)
+        assert caught, f"no pin catches the planted mistake: {what}"
