@@ -1,0 +1,103 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) attention-forward library.
+ *
+ * The library computes, for every (batch b, head h) and query row i,
+ *
+ *     O_i = sum_j softmax_j(scale * q_i . k_j  [ -inf where causal and j > i ]) * v_j
+ *     L_i = ln sum_j exp(scale * q_i . k_j)   (over the keys row i may see)
+ *
+ * without ever writing the N x N score matrix to device memory: query rows
+ * are taken 128 at a time, K/V tiles stream through shared memory, and an
+ * online-softmax state (running max m, running denominator l, output
+ * accumulator o, rescaled by exp(m_old - m_new) when the max rises) is
+ * carried per row, as "Kernels — fusion and FlashAttention" §3–§4 and
+ * "Fusion and IO-aware kernels" § FlashAttention (steps 1–4) describe.  The
+ * saved logsumexp is the m + log l statistic of "Kernels — fusion and
+ * FlashAttention" §5 and "Writing and Benchmarking Custom Kernels" §10.3.2,
+ * kept in fp32.
+ *
+ * Every function returns an fa_status; none throws, aborts or prints.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same type as cudaStream_t / CUstream); NULL is
+ * the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, non-finite or non-positive
+                                scale, causal not 0/1, o overlapping q/k/v/lse */
+    FA_ERR_UNSUPPORTED = 2,  /* head size not 64/128, pointer not 16-byte aligned
+                                (lse: 4-byte), device not sm_103 */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
+    FA_ERR_TIMEOUT = 4       /* a kernel gave up a pipeline wait (device status) */
+} fa_status;
+
+/*
+ * fa_fwd — attention forward on one GPU.
+ *
+ * Operation: see the file comment ("Kernels — fusion and FlashAttention" §2
+ * for the attention itself, §3 for the recurrence; "Writing and Benchmarking
+ * Custom Kernels" §10.3.1 for causal tile skipping and the masked last tile).
+ *
+ * Arguments
+ *   q, k, v  device pointers, bf16, contiguous (B, H, N, d) row-major, read only.
+ *   o        device pointer, bf16, contiguous (B, H, N, d); fully written.
+ *   lse      device pointer, fp32, contiguous (B, H, N); fully written with the
+ *            natural-log logsumexp of the scaled, masked scores of each row.
+ *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 1,
+ *            B*H*N*d < 2^62, B*H*ceil(N/128) < 2^31.
+ *   d        head size; 64 or 128.
+ *   causal   0: every query sees every key; 1: query i sees keys 0..i.
+ *   scale    finite, > 0 (typically 1/sqrt(d)); scores are scale * q.k.
+ *   stream   CUDA stream the work is enqueued on.
+ *
+ * Ownership: the caller allocates and frees every buffer.  The library keeps
+ * no per-call state and allocates no device memory; it caches one-time
+ * per-device set-up (kernel attributes).
+ *
+ * Asynchrony: returns after enqueuing; results are valid once `stream` has
+ * been synchronised.  Errors found before the launch are returned directly;
+ * a pipeline timeout inside the kernel is reported by fa_check_device_status.
+ * o and lse must not overlap q, k, v or each other (FA_ERR_INVALID_ARG).
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                 int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_check_device_status — synchronises `stream`, reads and clears the
+ * device-side status word of the current device.  Returns FA_ERR_TIMEOUT if a
+ * kernel launched since the last check gave up a bounded wait (its outputs are
+ * then incomplete), FA_ERR_CUDA if the copy or synchronisation failed, FA_OK
+ * otherwise.  `where`, if not NULL, receives the code of the first wait that
+ * gave up (0 if none).
+ */
+fa_status fa_check_device_status(fa_stream_t stream, uint32_t *where);
+
+/*
+ * fa_set_wait_limit_ns — upper bound, in nanoseconds, on any single pipeline
+ * wait inside the kernels launched after this call (default 1e9 = 1 s; 0
+ * restores the default).  Affects only how quickly a stuck kernel gives up.
+ */
+fa_status fa_set_wait_limit_ns(uint64_t ns);
+
+/* Static description of a status code (never NULL). */
+const char *fa_status_string(fa_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,137 @@
+"""GB300 (sm_103a) attention forward: Python binding of the C ABI in include/fa.h.
+
+Only argument marshalling happens here; every step of the computation runs in
+the CUDA kernels of ``libfa_gb300.so``.  There is no fallback: if the library
+is missing or the device is not sm_103, calls raise.
+
+    o, lse = io_aware_attention_gb300.fwd(q, k, v, causal=True)
+
+q, k, v: CUDA bf16 tensors of shape (B, H, N, d), contiguous, d in {64, 128}.
+Returns o (bf16, same shape) and lse (fp32, (B, H, N)), the natural-log
+logsumexp of each row's scaled, masked scores.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+__all__ = ["fwd", "fwd_into", "check_device_status", "set_wait_limit_ns", "FaError",
+           "library", "library_path", "version", "STATUS"]
+
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
+          4: "FA_ERR_TIMEOUT"}
+EXPORTS = ["fa_fwd", "fa_check_device_status", "fa_set_wait_limit_ns", "fa_status_string",
+           "fa_version"]
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        self.name = STATUS.get(code, f"status {code}")
+        super().__init__(f"{what}: {self.name}" if what else self.name)
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def library():
+    """Load ``libfa_gb300.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as "
+                           "g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp]
+    lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.fa_check_device_status.restype = ctypes.c_int
+    lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.fa_set_wait_limit_ns.restype = ctypes.c_int
+    lib.fa_status_string.argtypes = [ctypes.c_int]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def version() -> int:
+    return int(library().fa_version())
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(q, k, v):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bf16, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be (B, H, N, d), got shape {tuple(t.shape)}")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError(f"q, k, v shapes differ: {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+
+
+def fwd_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None):
+    """Runs the kernel into caller-provided ``o`` (bf16) and ``lse`` (fp32)."""
+    _check(q, k, v)
+    B, H, N, d = (int(s) for s in q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc = library().fa_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                          ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
+                          ctypes.c_void_p(lse.data_ptr()), B, H, N, d, int(bool(causal)),
+                          float(scale), _stream_handle(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_fwd")
+    return o, lse
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Attention forward; returns ``(o, lse)`` (see module docstring)."""
+    import torch
+
+    _check(q, k, v)
+    B, H, N, d = (int(s) for s in q.shape)
+    with torch.cuda.device(q.device):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+        return fwd_into(q, k, v, o, lse, causal, scale, stream)
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronises the stream and returns the device status (0 = ok, 4 = a wait
+    timed out); raises FaError on a CUDA error."""
+    where = ctypes.c_uint32(0)
+    rc = library().fa_check_device_status(_stream_handle(stream), ctypes.byref(where))
+    if rc == 3:
+        raise FaError(rc, "fa_check_device_status")
+    return rc
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    library().fa_set_wait_limit_ns(int(ns))

@@ -1,0 +1,198 @@
+// C ABI of the attention-forward library: argument checks, TMA descriptors,
+// kernel selection and launch.  Declarations and the contract: include/fa.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int FA_VERSION = 100;  // 0.1.0
+constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 1000000000ull;
+constexpr int MAX_DEVICES = 64;
+
+std::atomic<uint64_t> g_wait_limit_ns{DEFAULT_WAIT_LIMIT_NS};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// (B*H, N, d) bf16 viewed as a 3-D tensor (d innermost); box = 64 columns x
+// `rows` rows x 1 head, 128-byte swizzle.  Rows past N read as zero on loads
+// and are dropped on stores.
+bool make_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d, uint32_t rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(N * d * 2)};
+    cuuint32_t box[3] = {64, rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// Per-device, per-kernel one-time set-up (opt-in shared memory size).
+template <int D, bool CAUSAL>
+cudaError_t prepare_kernel(int dev)
+{
+    static std::atomic<int> done[MAX_DEVICES];
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)fa::Layout<D>::SMEM_BYTES);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+template <int D, bool CAUSAL>
+fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                 const CUtensorMap& mo, const fa::Params& p, unsigned grid, int dev,
+                 cudaStream_t stream)
+{
+    if (prepare_kernel<D, CAUSAL>(dev) != cudaSuccess) return FA_ERR_CUDA;
+    fa::fa_fwd_kernel<D, CAUSAL>
+        <<<grid, fa::NUM_THREADS, fa::Layout<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mo, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+bool device_is_sm103(int* dev_out)
+{
+    int dev = -1, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return false;
+    *dev_out = dev;
+    return major == 10 && minor == 3;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                 int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream)
+{
+    // ---- argument checks (no CUDA call before these pass)
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t LIM = (int64_t)1 << 62;
+    if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / d) return FA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    const int64_t m_blocks = (N + fa::BM - 1) / fa::BM;
+    if (BH > (((int64_t)1 << 31) - 1) / m_blocks) return FA_ERR_INVALID_ARG;
+    if (N > INT32_MAX || BH > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_UNSUPPORTED;
+    const size_t tb = (size_t)(BH * N * d * 2), lb = (size_t)(BH * N * 4);
+    if (overlaps(o, tb, q, tb) || overlaps(o, tb, k, tb) || overlaps(o, tb, v, tb) ||
+        overlaps(o, tb, lse, lb) || overlaps(lse, lb, q, tb) || overlaps(lse, lb, k, tb) ||
+        overlaps(lse, lb, v, tb))
+        return FA_ERR_INVALID_ARG;
+
+    // ---- device
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_map(&mq, q, BH, N, d, fa::BM) || !make_map(&mk, k, BH, N, d, fa::BN) ||
+        !make_map(&mv, v, BH, N, d, fa::BN) || !make_map(&mo, o, BH, N, d, fa::BM))
+        return FA_ERR_CUDA;
+
+    fa::Params p;
+    p.lse = lse;
+    p.N = (int)N;
+    p.num_m_blocks = (int)m_blocks;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    const unsigned grid = (unsigned)(BH * m_blocks);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    if (d == 128)
+        return causal ? launch<128, true>(mq, mk, mv, mo, p, grid, dev, st)
+                      : launch<128, false>(mq, mk, mv, mo, p, grid, dev, st);
+    return causal ? launch<64, true>(mq, mk, mv, mo, p, grid, dev, st)
+                  : launch<64, false>(mq, mk, mv, mo, p, grid, dev, st);
+}
+
+fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
+{
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int h[2] = {0u, 0u};
+    const unsigned int zero[2] = {0u, 0u};
+    if (cudaMemcpyFromSymbolAsync(&h[0], fa::g_status, sizeof(unsigned int), 0,
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyFromSymbolAsync(&h[1], fa::g_status_where, sizeof(unsigned int), 0,
+                                  cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (where) *where = h[1];
+    if (h[0] != 0u) {
+        if (cudaMemcpyToSymbolAsync(fa::g_status, &zero[0], sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyToSymbolAsync(fa::g_status_where, &zero[1], sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return FA_ERR_CUDA;
+        return FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+fa_status fa_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_limit_ns.store(ns ? ns : DEFAULT_WAIT_LIMIT_NS, std::memory_order_relaxed);
+    return FA_OK;
+}
+
+const char* fa_status_string(fa_status s)
+{
+    switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported (head size, alignment or device)";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+int fa_version(void) { return FA_VERSION; }
+
+}  // extern "C"

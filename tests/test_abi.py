@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports what include/fa.h declares, and
+rejects bad arguments before touching the GPU (no compute call is made)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import io_aware_attention_gb300 as fa
+from io_aware_attention_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "fa.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(_build.LIB_PATH),
+                                reason="neither nvcc nor a built library")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        s = lib.fa_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.fa_status_string(99) == b"unknown status"
+    assert fa.version() >= 100
+
+
+P = 1 << 20  # fake, 16-byte aligned "device" addresses: never dereferenced
+
+
+def call(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, N=16, d=64, causal=0,
+         scale=0.125):
+    vp = ctypes.c_void_p
+    return lib.fa_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, N, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(d=0), 1),
+    (dict(causal=2), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=0.0), 1), (dict(scale=-0.1), 1),
+    (dict(d=96), 2), (dict(d=256), 2),
+    (dict(q=P + 8), 2), (dict(o=4 * P + 4), 2), (dict(lse=5 * P + 2), 2),
+    (dict(o=P), 1),                       # o aliases q
+    (dict(o=3 * P + 16), 1),              # o overlaps the tail of v
+    (dict(lse=4 * P + 64), 1),            # lse inside o
+    (dict(B=1 << 40, H=1 << 20), 1),      # element count overflows
+])
+def test_bad_arguments_are_rejected(lib, kw, status):
+    assert call(lib, **kw) == status
+
+
+def test_wait_limit_setter(lib):
+    assert lib.fa_set_wait_limit_ns(5_000_000) == 0
+    assert lib.fa_set_wait_limit_ns(0) == 0  # back to the default

@@ -1,0 +1,109 @@
+"""GPU kernel vs the fp64 oracle on small shapes, element by element.
+
+Shapes span several 128-row tiles and ragged tails (N not a multiple of the
+tile, "Writing and Benchmarking Custom Kernels" §10.3.1: the final partial
+tile), both head sizes, causal and not, plus the method's degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import io_aware_attention_gb300 as fa
+import oracle
+from io_aware_attention_gb300.workloads import make_random_qkv
+
+from _parity import assert_close, run_guarded
+
+pytestmark = pytest.mark.gpu
+
+NS = [1, 2, 17, 64, 127, 128, 129, 200, 256, 383, 640]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", NS)
+def test_small_shapes(N, d, causal):
+    q, k, v = make_random_qkv(1, 2, N, d, seed=100 + N + d)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_guarded(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale)
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+                 f"N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_heads(d):
+    q, k, v = make_random_qkv(3, 5, 300, d, seed=7)
+    for causal in (False, True):
+        o, lse = run_guarded(q.cuda(), k.cuda(), v.cuda(), causal, 0.1)
+        o_ref, lse_ref = oracle.attention(q, k, v, causal, 0.1)
+        assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"d={d} {causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_row0_is_v0(d):
+    """Row 0 sees key 0 only: O_0 = V_0 bit for bit, L_0 = scale * q_0 . k_0."""
+    q, k, v = make_random_qkv(2, 3, 257, d, seed=8)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o[:, :, 0].cpu(), v[:, :, 0])
+    ref = scale * (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1)
+    assert (lse[:, :, 0].cpu().double() - ref).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_last_row_equals_full_row(d):
+    q, k, v = make_random_qkv(1, 4, 333, d, seed=9)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    oc, lc = fa.fwd(qc, kc, vc, causal=True)
+    on, ln = fa.fwd(qc, kc, vc, causal=False)
+    torch.cuda.synchronize()
+    assert (oc[:, :, -1].float() - on[:, :, -1].float()).abs().max().item() <= 1e-2
+    assert (lc[:, :, -1] - ln[:, :, -1]).abs().max().item() <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_stress(d, causal):
+    """Large scores whose row max jumps late in the row (Q x4, every 64th key x8
+    and the last key x16): the running max must rescale O and l."""
+    q, k, v = make_random_qkv(1, 2, 1000, d, seed=10, q_mult=4.0)
+    k = k.clone()
+    k[:, :, 63::64] *= 8
+    k[:, :, -1] *= 16
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_guarded(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale)
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "stress")
+
+
+def test_constant_values_pass_through():
+    q, k, _ = make_random_qkv(1, 2, 500, 128, seed=11)
+    v = torch.full_like(q, 0.7109375)  # exactly representable in bf16
+    o, _ = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    torch.cuda.synchronize()
+    assert (o.float() - 0.7109375).abs().max().item() <= 2 ** -8
+
+
+def test_side_stream_and_repeatability():
+    q, k, v = (t.cuda() for t in make_random_qkv(2, 2, 700, 128, seed=12))
+    o1, l1 = fa.fwd(q, k, v, causal=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, l2 = fa.fwd(q, k, v, causal=True)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_python_checks_reject_bad_tensors():
+    q, k, v = (t.cuda() for t in make_random_qkv(1, 1, 64, 64, seed=13))
+    with pytest.raises(ValueError):
+        fa.fwd(q.float(), k, v)
+    with pytest.raises(ValueError):
+        fa.fwd(q.transpose(2, 3), k, v)
+    with pytest.raises(fa.FaError) as e:
+        fa.fwd(q[..., :32].contiguous(), k[..., :32].contiguous(), v[..., :32].contiguous())
+    assert e.value.code == 2
