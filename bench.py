@@ -1,0 +1,380 @@
+"""Throughput of the attention forward on GB300, as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--batch B] [--no-cpu]
+
+A step is one fa_fwd launch over the whole workload (default: B=8, H=32,
+N=4096, d=128, causal -- the pages' B = 8, h = 32 example).  The metric is
+attention-forward TFLOP/s with 4·B·H·N²·d FLOPs per step, halved under the
+causal mask.
+
+* value: inputs resident in HBM; K launches timed with CUDA events on the
+  launching stream between two barriers + synchronisations; max over ranks.
+  Inputs (Q, K, V: 805 MB at the default workload) are larger than L2, so no
+  extra flush is made between launches.
+* e2e: the same metric through the public call with host buffers: every step
+  copies Q, K, V from pinned host memory to the device, runs fa_fwd and copies
+  O and the logsumexp back.
+* roofline: the attention kernel is tensor-core bound; achieved = algorithmic
+  FLOPs per launch / mean launch time, against the measured bf16 GEMM peak.
+* cpu_baseline: the fp64 CPU oracle timed on the host cores over a bounded
+  sample of rows of the same workload (rank 0 only).
+* --impl reference: the oracle alone (the reference arm: the pages ship no
+  runnable code), each step a bounded sample of rows.
+
+With N > 1 (torchrun) every rank runs its own copy of the workload on its own
+GPU: the (batch, head) problems are independent, so there is no data-path
+collective ("scaling": "weak"); only the timing barrier and the max-over-ranks
+reduction communicate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak, causal & non-causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling captures)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
+    """Times the fp64 oracle on a bounded sample of rows; returns a dict with
+    TFLOP/s, the threads used and a description of the sample."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+
+    def flops_of(rows):
+        vis = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        return float(np.sum(4.0 * w.d * vis))
+
+    def run(n):
+        bh = rng.integers(0, w.B * w.H, size=n, dtype=np.int64)
+        row = rng.integers(0, w.N, size=n, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.causal, w.scale, bh, row)
+        return time.perf_counter() - t0, flops_of(row)
+
+    threads = oracle.max_threads()
+    n = 32
+    dt, fl = run(n)
+    while dt < 0.5 and n < (1 << 20):  # calibrate
+        n *= 4
+        dt, fl = run(n)
+    rate = fl / dt
+    total_n = n
+    total_t = dt
+    total_f = fl
+    n_big = max(n, int(n * (budget_s - total_t) / max(dt, 1e-9)))
+    if total_t < budget_s:
+        dt, fl = run(n_big)
+        total_n, total_t, total_f = n_big, dt, fl
+        rate = fl / dt
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{total_n} random (b,h,row) rows of the same workload, fp64, "
+                      f"{total_t:.1f} s; FLOPs = 4*d*visible keys per row"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    from io_aware_attention_gb300 import iomodel
+    from io_aware_attention_gb300.workloads import HEADLINE, WORKLOADS, Workload
+
+    wname = args.workload or HEADLINE
+    w = WORKLOADS[wname]
+    if args.batch:
+        w = Workload(w.name + f"_b{args.batch}", args.batch, w.H, w.N, w.d, w.causal, w.seed,
+                     w.q_mult, w.spike_every, w.spike_mult, w.sample_rows)
+    flops = iomodel.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+              "scale": "1/sqrt(d)", "inputs": "Q,K,V iid N(0,1) bf16, seeded",
+              "per_gpu_problem": True, "parallelism": f"replicas x{args.gpus}",
+              "l2": f"inputs {3 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB > 129 MB L2 (no flush)"}
+
+    if args.impl == "reference":
+        return run_reference(args, w, flops, config, rank, world)
+
+    import torch
+    import torch.distributed as distm
+
+    import io_aware_attention_gb300 as fa
+    from io_aware_attention_gb300.workloads import make_qkv
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        distm.init_process_group("nccl", device_id=dev)
+        pg = True
+
+    def barrier():
+        if pg:
+            distm.barrier()
+
+    q_h, k_h, v_h = make_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(args.warmup, 3)):
+        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+    torch.cuda.synchronize()
+    if fa.check_device_status() != 0:
+        raise RuntimeError("kernel reported a timed-out wait during warm-up")
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = ev0.elapsed_time(ev1)
+    if fa.check_device_status() != 0:
+        raise RuntimeError("kernel reported a timed-out wait in the timed region")
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        distm.all_reduce(t, op=distm.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if pg:
+            t = torch.tensor([ems], device=dev)
+            distm.all_reduce(t, op=distm.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": flops * world / (ems / n_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": ems / n_e2e, "steps": n_e2e, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    peaks, peak_src = load_peaks()
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
+            "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+            "kernel": f"fa::fa_fwd_kernel<{w.d},{str(w.causal).lower()}>",
+            "traffic": None,
+            "alg_bytes_per_launch": iomodel.attention_min_bytes(w.B, w.H, w.N, w.d),
+            "alg_flops_per_launch": flops}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_oracle_rate(w, q_h, k_h, v_h, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3),
+                "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": clocks,
+                "pct_of_peak": round(100 * achieved / peak, 2)}
+        print(json.dumps(line), flush=True)
+    if pg:
+        distm.destroy_process_group()
+    return 0
+
+
+def run_reference(args, w, flops_full, config, rank, world):
+    """The reference arm: the fp64 CPU oracle, timed on the host cores, each
+    step a bounded random sample of rows of the same workload."""
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from io_aware_attention_gb300.workloads import make_qkv
+
+    q, k, v = make_qkv(w)
+    rng = np.random.default_rng(99)
+    steps, warm = args.steps, max(args.warmup, 3)
+    per_step_budget = min(0.25, 90.0 / max(1, steps + warm))
+
+    def sample(n):
+        return (rng.integers(0, w.B * w.H, size=n, dtype=np.int64),
+                rng.integers(0, w.N, size=n, dtype=np.int64))
+
+    def step(n):
+        bh, row = sample(n)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.causal, w.scale, bh, row)
+        dt = time.perf_counter() - t0
+        vis = (row + 1) if w.causal else np.full_like(row, w.N)
+        return dt, float(np.sum(4.0 * w.d * vis))
+
+    n = 8
+    dt, _ = step(n)
+    while dt < per_step_budget / 4 and n < (1 << 18):
+        n *= 2
+        dt, _ = step(n)
+    n = max(1, int(n * per_step_budget / max(dt, 1e-9)))
+    for _ in range(warm):
+        step(n)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(steps):
+        dt, fl = step(n)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{n} random (b,h,row) rows per step, fp64 two-pass "
+                                       "oracle; FLOPs = 4*d*visible keys per row"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

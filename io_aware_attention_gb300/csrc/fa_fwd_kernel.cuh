@@ -8,9 +8,10 @@
 //   S_j   = Q K_j^T                        (tcgen05.mma, smem x smem -> TMEM fp32)
 //   m_new = max(m, rowmax(S_j) * c)        (c = scale * log2 e, base-2 units)
 //   P_j   = 2^(S_j * c - m)                (bf16, written back into TMEM)
-//   l     = l * 2^(m_old - m_new) + rowsum(P_j)
+//   l     = l * 2^(m_old - m_new) + rowsum(P_j)          (fp32 values)
+//   l~    = l~ * 2^(m_old - m_new) + rowsum(bf16(P_j))   (the values the MMA sees)
 //   O     = O * 2^(m_old - m_new) + P_j V_j (tcgen05.mma, TMEM x smem -> TMEM fp32)
-//   out   = O / l,   lse = (m + log2 l) * ln 2
+//   out   = O / l~,   lse = (m + log2 l) * ln 2
 //
 // The score matrix lives only in TMEM, one 128x128 tile at a time.
 //
@@ -29,7 +30,11 @@
 //
 // Rescaling is lazy: a row keeps its reference max until a tile raises the
 // max by more than RESCALE_LOG2 (base-2 units); P and l always share the same
-// reference, so O / l is unaffected and P stays below 2^RESCALE_LOG2.
+// reference, so O / l is unaffected and P stays below 2^RESCALE_LOG2.  Because
+// the reference can sit below the row max, the dominant probability is not
+// exactly 1 and its bf16 rounding would not cancel against an fp32 l; O is
+// therefore divided by l~, the sum of the rounded probabilities (O is then an
+// exact convex combination of the value rows), while the logsumexp uses l.
 //
 // Every wait is bounded in time; on expiry the thread records the wait in the
 // device status word, raises a CTA-wide abort flag, and all roles drain their
@@ -305,7 +310,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
         const float sl2 = p.scale_log2;
         float m_ref = -INFINITY;
-        float l = 0.f;
+        float l = 0.f;   // sum of fp32 probabilities (logsumexp)
+        float lr = 0.f;  // sum of the bf16-rounded probabilities (normalises O)
         bool ok = true;
 
         for (int j = 0; j < n_kv; ++j) {
@@ -359,6 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_after_sync();
                     const float corr = ptx::ex2(m_ref - m_new);
                     l *= corr;
+                    lr *= corr;
                     m_ref = m_new;
 #pragma unroll
                     for (int ch = 0; ch < D / 32; ++ch) {
@@ -373,11 +380,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
 
-            // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA; l sums the
-            // fp32 values, so the logsumexp carries no bf16 rounding.
+            // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.
             const float neg_m = -m_ref;
             uint32_t pk0[32], pk1[32];
-            float rs0 = 0.f, rs1 = 0.f;
+            float rs0 = 0.f, rs1 = 0.f, rr0 = 0.f, rr1 = 0.f;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const float a0 = ptx::ex2(fmaf(s[2 * c], sl2, neg_m));
@@ -386,10 +392,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float b1 = ptx::ex2(fmaf(s[64 + 2 * c + 1], sl2, neg_m));
                 rs0 += a0 + a1;
                 rs1 += b0 + b1;
-                pk0[c] = ptx::pack_bf16x2(a0, a1);
-                pk1[c] = ptx::pack_bf16x2(b0, b1);
+                const uint32_t w0 = ptx::pack_bf16x2(a0, a1);
+                const uint32_t w1 = ptx::pack_bf16x2(b0, b1);
+                rr0 += __uint_as_float(w0 << 16) + __uint_as_float(w0 & 0xffff0000u);
+                rr1 += __uint_as_float(w1 << 16) + __uint_as_float(w1 & 0xffff0000u);
+                pk0[c] = w0;
+                pk1[c] = w1;
             }
             l += rs0 + rs1;
+            lr += rr0 + rr1;
 
             // P buffer b was last read by the MMA of tile j-2.
             if (j >= 2) {
@@ -414,7 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (ok) {
             ptx::tc_fence_after_sync();
-            const float inv_l = 1.0f / l;
+            const float inv_l = 1.0f / lr;
             // O row -> bf16 -> the Q tile's shared memory (Q is no longer read),
             // in the 128-byte-swizzled layout the O tensor map expects.
 #pragma unroll
