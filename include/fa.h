@@ -77,7 +77,8 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
  * fa_check_device_status — synchronises `stream`, reads and clears the
  * device-side status word of the current device.  Returns FA_ERR_TIMEOUT if a
  * kernel launched since the last check gave up a bounded wait (its outputs are
- * then incomplete), FA_ERR_CUDA if the copy or synchronisation failed, FA_OK
+ * then incomplete), FA_ERR_CUDA if the copy or synchronisation failed or a
+ * kernel refused to run (shared memory not 1024-byte aligned), FA_OK
  * otherwise.  `where`, if not NULL, receives the code of the first wait that
  * gave up (0 if none).
  */

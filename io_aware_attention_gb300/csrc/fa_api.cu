@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -77,13 +78,23 @@ cudaError_t prepare_kernel(int dev)
 
 template <int D, bool CAUSAL>
 fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                 const CUtensorMap& mo, const fa::Params& p, unsigned grid, int dev,
-                 cudaStream_t stream)
+                 const fa::Params& p, unsigned grid, int dev, cudaStream_t stream)
 {
     if (prepare_kernel<D, CAUSAL>(dev) != cudaSuccess) return FA_ERR_CUDA;
     fa::fa_fwd_kernel<D, CAUSAL>
-        <<<grid, fa::NUM_THREADS, fa::Layout<D>::SMEM_BYTES, stream>>>(mq, mk, mv, mo, p);
+        <<<grid, fa::NUM_THREADS, fa::Layout<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Number of SMs of a device (cached): the kernel is persistent, one CTA per SM.
+int sm_count(int dev)
+{
+    static std::atomic<int> cache[MAX_DEVICES];
+    if (dev < 0 || dev >= MAX_DEVICES) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 bool device_is_sm103(int* dev_out)
@@ -130,25 +141,30 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     int dev = -1;
     if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
 
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_map(&mq, q, BH, N, d, fa::BM) || !make_map(&mk, k, BH, N, d, fa::BN) ||
-        !make_map(&mv, v, BH, N, d, fa::BN) || !make_map(&mo, o, BH, N, d, fa::BM))
+        !make_map(&mv, v, BH, N, d, fa::BN))
         return FA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
 
     fa::Params p;
+    p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.N = (int)N;
     p.num_m_blocks = (int)m_blocks;
+    p.num_items = (int)(BH * m_blocks);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-    const unsigned grid = (unsigned)(BH * m_blocks);
+    // One CTA per SM, at most one per pair of work items.
+    const unsigned grid = (unsigned)std::min<int64_t>((BH * m_blocks + 1) / 2, sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     if (d == 128)
-        return causal ? launch<128, true>(mq, mk, mv, mo, p, grid, dev, st)
-                      : launch<128, false>(mq, mk, mv, mo, p, grid, dev, st);
-    return causal ? launch<64, true>(mq, mk, mv, mo, p, grid, dev, st)
-                  : launch<64, false>(mq, mk, mv, mo, p, grid, dev, st);
+        return causal ? launch<128, true>(mq, mk, mv, p, grid, dev, st)
+                      : launch<128, false>(mq, mk, mv, p, grid, dev, st);
+    return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st)
+                  : launch<64, false>(mq, mk, mv, p, grid, dev, st);
 }
 
 fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
@@ -164,13 +180,14 @@ fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
         return FA_ERR_CUDA;
     if (where) *where = h[1];
     if (h[0] != 0u) {
+        const fa_status st_code = (h[0] & fa::STATUS_TIMEOUT) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
         if (cudaMemcpyToSymbolAsync(fa::g_status, &zero[0], sizeof(unsigned int), 0,
                                     cudaMemcpyHostToDevice, st) != cudaSuccess ||
             cudaMemcpyToSymbolAsync(fa::g_status_where, &zero[1], sizeof(unsigned int), 0,
                                     cudaMemcpyHostToDevice, st) != cudaSuccess ||
             cudaStreamSynchronize(st) != cudaSuccess)
             return FA_ERR_CUDA;
-        return FA_ERR_TIMEOUT;
+        return st_code;
     }
     return FA_OK;
 }
@@ -194,5 +211,14 @@ const char* fa_status_string(fa_status s)
 }
 
 int fa_version(void) { return FA_VERSION; }
+
+#ifdef FA_TRACE
+// Trace builds only: points the kernels' event trace at a device buffer.
+int fa_debug_set_trace(void* device_buffer)
+{
+    unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+    return cudaMemcpyToSymbol(fa::g_trace, &p, sizeof p) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 }  // extern "C"
