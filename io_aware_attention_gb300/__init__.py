@@ -18,13 +18,13 @@ import os
 
 from . import _build
 
-__all__ = ["fwd", "fwd_into", "check_device_status", "set_wait_limit_ns", "FaError",
+__all__ = ["fwd", "fwd_into", "check_device_status", "set_wait_limit_ns", "debug_skip_k_tile", "FaError",
            "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT"}
-EXPORTS = ["fa_fwd", "fa_check_device_status", "fa_set_wait_limit_ns", "fa_status_string",
-           "fa_version"]
+EXPORTS = ["fa_fwd", "fa_check_device_status", "fa_set_wait_limit_ns", "fa_debug_skip_k_tile",
+           "fa_status_string", "fa_version"]
 
 
 class FaError(RuntimeError):
@@ -58,6 +58,8 @@ def library():
     lib.fa_check_device_status.restype = ctypes.c_int
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.fa_set_wait_limit_ns.restype = ctypes.c_int
+    lib.fa_debug_skip_k_tile.argtypes = [ctypes.c_int]
+    lib.fa_debug_skip_k_tile.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
@@ -135,3 +137,10 @@ def check_device_status(stream=None) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     library().fa_set_wait_limit_ns(int(ns))
+
+
+def debug_skip_k_tile(tile: int) -> None:
+    """Test hook: see fa_debug_skip_k_tile in include/fa.h (-1 turns it off)."""
+    rc = library().fa_debug_skip_k_tile(int(tile))
+    if rc != 0:
+        raise FaError(rc, "fa_debug_skip_k_tile")

@@ -19,6 +19,7 @@ constexpr uint64_t DEFAULT_WAIT_LIMIT_NS = 1000000000ull;
 constexpr int MAX_DEVICES = 64;
 
 std::atomic<uint64_t> g_wait_limit_ns{DEFAULT_WAIT_LIMIT_NS};
+std::atomic<int> g_debug_skip_k{-1};
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -156,6 +157,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.num_items = (int)(BH * m_blocks);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.debug_skip_k = g_debug_skip_k.load(std::memory_order_relaxed);
     // One CTA per SM, at most one per pair of work items.
     const unsigned grid = (unsigned)std::min<int64_t>((BH * m_blocks + 1) / 2, sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -195,6 +197,13 @@ fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
 fa_status fa_set_wait_limit_ns(uint64_t ns)
 {
     g_wait_limit_ns.store(ns ? ns : DEFAULT_WAIT_LIMIT_NS, std::memory_order_relaxed);
+    return FA_OK;
+}
+
+fa_status fa_debug_skip_k_tile(int tile)
+{
+    if (tile < -1) return FA_ERR_INVALID_ARG;
+    g_debug_skip_k.store(tile, std::memory_order_relaxed);
     return FA_OK;
 }
 

@@ -74,6 +74,7 @@ constexpr int NUM_THREADS = SOFTMAX_THREADS + 64;
 constexpr int WARP_TMA = 8;
 constexpr int WARP_MMA = 9;
 constexpr float RESCALE_LOG2 = 8.0f;
+constexpr uint32_t WAIT_SLEEP_NS = 20000;  // suspend-time hint of one poll
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_LX = 400;
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t BLK_BYTES = BN * 128;  // one 64-column, 128-row swizzled block (16 KB)
@@ -93,6 +94,7 @@ struct Params {
     int num_items;
     float scale_log2;  // scale * log2(e)
     unsigned long long wait_limit_ns;
+    int debug_skip_k;  // test hook: global K tile the producer never loads (-1: none)
 };
 
 template <int D>
@@ -164,16 +166,17 @@ __device__ __forceinline__ void record_timeout(uint32_t code, volatile uint32_t*
 
 // Bounded wait on an mbarrier phase.  Gives up (returns false) when the CTA
 // has aborted or after `limit_ns`, in which case it raises the abort.  The
-// abort flag and the clock are looked at only every 256 polls; try_wait
-// suspends the thread until the phase completes (or a short hardware time
-// limit), so waiting threads leave their issue slots to the others.
+// abort flag and the clock are looked at only every 256 polls.  A waiting
+// thread sleeps in try_wait (woken when the phase completes) rather than
+// spinning: a spinning warp takes issue slots from the warps on its SM
+// sub-partition, among them the single thread that issues the MMAs.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                          volatile uint32_t* abort_flag, uint32_t code)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = 0;
     for (uint32_t polls = 1;; ++polls) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
         if ((polls & 255u) == 0u) {
             if (*abort_flag) return false;
             const uint64_t t = ptx::globaltimer_ns();
@@ -384,6 +387,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t ph = (uint32_t)(gk / L::KSTAGES) & 1u;
                     if (!(ok = wait_bar(bar(L::B_KEMPTY + s), ph ^ 1u, limit, abort_flag, 0x100 + L::B_KEMPTY + s)))
                         break;
+                    if (gk == p.debug_skip_k && blockIdx.x == 0) {
+                        // Test hook: this K tile is never loaded, so the wait of
+                        // the MMA warp on it runs out (exercises the abort path).
+                        v_bh[gk % 3] = it.bh;
+                        v_j[gk % 3] = j;
+                        ++gk;
+                        if (gv <= gk - 3) ok = issue_v();
+                        continue;
+                    }
                     ptx::mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::KV_BYTES);
                     FA_TRACE_EV(8, gk, 0);
                     for (int c = 0; c < L::DBLK; ++c)
@@ -401,13 +413,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Drain: every copy this thread issued must land before exit.
             if (k > 0) drain_bar(bar(L::B_QFULL), (uint32_t)((k - 1) & 1), limit, abort_flag, 0x180);
             for (int g = max(0, gk - L::KSTAGES); g < gk; ++g)
-                drain_bar(bar(L::B_KFULL + g % L::KSTAGES), (uint32_t)(g / L::KSTAGES) & 1u, limit,
-                          abort_flag, 0x181);
+                if (!(g == p.debug_skip_k && blockIdx.x == 0))
+                    drain_bar(bar(L::B_KFULL + g % L::KSTAGES), (uint32_t)(g / L::KSTAGES) & 1u, limit,
+                              abort_flag, 0x181);
             for (int g = max(0, gv - L::VSTAGES); g < gv; ++g)
                 drain_bar(bar(L::B_VFULL + g % L::VSTAGES), (uint32_t)(g / L::VSTAGES) & 1u, limit,
                           abort_flag, 0x182);
         }
-        __syncwarp();
+        // Lanes 1-31 go straight to the closing __syncthreads: parked on a
+        // CTA barrier they do not compete with lane 0 for the warp's issue.
     } else if (warp == WARP_MMA) {
         // -------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -447,6 +461,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // BLK_BYTES apart (the ones block follows the value blocks), 8-key
             // groups 1024 bytes apart.
             auto issue_pv = [&](int gp, bool first) -> bool {
+                FA_TRACE_EV(9, gp, 6);
                 const int b = gp & 1;
                 const int s = gp % L::VSTAGES;
                 if (!wait_bar(bar(L::B_PFULL + b), (uint32_t)(gp >> 1) & 1u, limit, abort_flag,
@@ -461,10 +476,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
                 const uint32_t p_tmem = tmem + (b ? TM_S1 : TM_S0);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
+                for (int kk = 0; kk < BN / 16; ++kk) {
                     ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
                                 v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
                                 (!first || kk > 0) ? 1u : 0u);
+                    if (kk == 0) FA_TRACE_EV(9, gp, 5);
+                    if (kk == 7) FA_TRACE_EV(9, gp, 7);
+                }
                 ptx::tc_commit(bar(L::B_VEMPTY + s));
                 ptx::tc_commit(bar(L::B_ODONE));
                 FA_TRACE_EV(9, gp, 4);
@@ -500,7 +518,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tc_commit(bar(L::B_DRAIN));
             drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
         }
-        __syncwarp();
     } else {
         // ---------------------------------------------------- softmax warps
         const int quarter = warp & 3;

@@ -55,6 +55,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended for up to `hint_ns`
+// (it is woken when the phase completes), so a waiting warp leaves its issue
+// slots to the warps it is waiting for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Non-blocking test of a phase (never suspends the thread).
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
 {

@@ -73,3 +73,9 @@ def test_bad_arguments_are_rejected(lib, kw, status):
 def test_wait_limit_setter(lib):
     assert lib.fa_set_wait_limit_ns(5_000_000) == 0
     assert lib.fa_set_wait_limit_ns(0) == 0  # back to the default
+
+
+def test_debug_hook_setter(lib):
+    assert lib.fa_debug_skip_k_tile(-2) == 1
+    assert lib.fa_debug_skip_k_tile(3) == 0
+    assert lib.fa_debug_skip_k_tile(-1) == 0
