@@ -219,10 +219,15 @@ def main(argv=None):
         w = Workload(w.name + f"_b{args.batch}", args.batch, w.H, w.N, w.d, w.causal, w.seed,
                      w.q_mult, w.spike_every, w.spike_mult, w.sample_rows)
     flops = iomodel.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    inputs = "Q,K,V iid N(0,1) bf16, seeded"
+    if w.q_mult != 1.0 or w.spike_every:
+        inputs += f"; Q x{w.q_mult:g}; every {w.spike_every}th key row x{w.spike_mult:g}"
+    in_mb = 3 * w.B * w.H * w.N * w.d * 2 / 1e6
     config = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-              "scale": "1/sqrt(d)", "inputs": "Q,K,V iid N(0,1) bf16, seeded",
+              "scale": "1/sqrt(d)", "inputs": inputs,
               "per_gpu_problem": True, "parallelism": f"replicas x{args.gpus}",
-              "l2": f"inputs {3 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB > 129 MB L2 (no flush)"}
+              "l2": (f"inputs {in_mb:.0f} MB > 129 MB L2 (no flush)" if in_mb > 129 else
+                     f"inputs {in_mb:.1f} MB fit in L2 (not flushed: warm-cache figure)")}
 
     if args.impl == "reference":
         return run_reference(args, w, flops, config, rank, world)
@@ -278,6 +283,22 @@ def main(argv=None):
         distm.all_reduce(t, op=distm.ReduceOp.MAX)
         ms = float(t.item())
     ms_per_step = ms / args.steps
+
+    # Spread of single launches (each bracketed by its own events), after the
+    # timed region: median and standard deviation.
+    singles = []
+    for _ in range(30):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+        b.record(stream)
+        singles.append((a, b))
+    torch.cuda.synchronize()
+    single_ms = [a.elapsed_time(b) for a, b in singles]
+    launch_stats = {"n": len(single_ms), "median_ms": round(statistics.median(single_ms), 5),
+                    "stdev_ms": round(statistics.stdev(single_ms), 5),
+                    "min_ms": round(min(single_ms), 5)}
     value = flops * world / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public call with host buffers
@@ -341,7 +362,7 @@ def main(argv=None):
                 "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": args.steps, "clocks": clocks,
+                "gpu_launches": args.steps, "clocks": clocks, "launch_stats": launch_stats,
                 "pct_of_peak": round(100 * achieved / peak, 2)}
         print(json.dumps(line), flush=True)
     if pg:

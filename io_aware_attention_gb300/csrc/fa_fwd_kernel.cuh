@@ -541,7 +541,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
             const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
             float m_ref = -INFINITY;
-            float lsum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // this half-row's sum of probabilities
+            // This half-row's sum of probabilities, as four packed fp32 pairs.
+            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
 
             for (int j = 0; j < it.n_kv; ++j, ++g) {
                 const int b = g & 1;
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tc_fence_after_sync();
                         const float corr = ptx::ex2(m_ref - m_new);
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) lsum[c] *= corr;
+                        for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
                         m_ref = m_new;
                         scale_cols<D>(o_cols, corr);
                         uint32_t lt[8];
@@ -615,14 +616,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
 
-                // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.
-                const float neg_m = -m_ref;
+                // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
+                // scaling and the sums use packed fp32x2 instructions: fewer
+                // issue slots, which the MMA issuer on the same sub-partition
+                // needs.
+                const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+                const uint64_t neg_m2 = ptx::f2_pack(-m_ref, -m_ref);
                 uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const float a0 = ptx::ex2(fmaf(s[2 * c], sl2, neg_m));
-                    const float a1 = ptx::ex2(fmaf(s[2 * c + 1], sl2, neg_m));
-                    lsum[c & 7] += a0 + a1;
+                    float x0, x1;
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2), x0, x1);
+                    const float a0 = ptx::ex2(x0);
+                    const float a1 = ptx::ex2(x1);
+                    lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
                     pk[c] = ptx::pack_bf16x2(a0, a1);
                 }
                 if (lane == 0) FA_TRACE_EV(warp, g, 3);
@@ -643,7 +650,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
                                        0x380 + L::B_OFINAL);
             ++kitem;
-            const float l_half = ((lsum[0] + lsum[1]) + (lsum[2] + lsum[3])) + ((lsum[4] + lsum[5]) + (lsum[6] + lsum[7]));
+            float l_lo, l_hi;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
+            const float l_half = l_lo + l_hi;
             // The two halves' fp32 sums meet in two spare TMEM columns (all of
             // this item's MMAs are complete).
             if (ok) {

@@ -54,6 +54,7 @@ WORKLOADS = {
         Workload("b1_h2_n256_d64", 1, 2, 256, 64, False, 1001),
         Workload("b4_h16_n2048_d128_causal", 4, 16, 2048, 128, True, 1002),
         Workload("b8_h32_n4096_d128_causal", 8, 32, 4096, 128, True, 1003, sample_rows=512),
+        Workload("b8_h32_n4096_d128", 8, 32, 4096, 128, False, 1006, sample_rows=512),
         Workload("b1_h32_n32768_d128_causal", 1, 32, 32768, 128, True, 1004, sample_rows=256),
         Workload("b16_h16_n8192_d64_spiky", 16, 16, 8192, 64, False, 1005, q_mult=4.0,
                  spike_every=512, spike_mult=8.0, sample_rows=512),
