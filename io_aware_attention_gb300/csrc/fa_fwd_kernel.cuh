@@ -351,173 +351,190 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == WARP_TMA) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            // K of global tile g is issued, then V of tile g-2 of the same
-            // item: the score MMA needs K a whole softmax step before the P.V
-            // MMA needs V.  The (head, key tile) of the last three K tiles are
-            // remembered for V.
-            int gk = 0, gv = 0, k = 0;
-            int v_bh[3] = {0, 0, 0}, v_j[3] = {0, 0, 0};
-            bool ok = true;
-            auto issue_v = [&]() -> bool {
-                const int s = gv % L::VSTAGES;
-                const uint32_t ph = (uint32_t)(gv / L::VSTAGES) & 1u;
-                if (!wait_bar(bar(L::B_VEMPTY + s), ph ^ 1u, limit, abort_flag, 0x100 + L::B_VEMPTY + s))
-                    return false;
+        // The whole warp runs the loop (warp-uniform control flow, so the
+        // compiler keeps its bookkeeping on the uniform datapath); one elected
+        // lane issues each copy.  K of global tile g is issued, then V of tile
+        // g-2 of the same item: the score MMA needs K a whole softmax step
+        // before the P.V MMA needs V.  The (head, key tile) of the last three
+        // K tiles are remembered for V.
+        int gk = 0, gv = 0, k = 0;
+        int vb0 = 0, vb1 = 0, vb2 = 0, vj0 = 0, vj1 = 0, vj2 = 0;
+        bool ok = true;
+        auto remember = [&](int g, int bh, int j) {
+            const int r = g % 3;
+            vb0 = (r == 0) ? bh : vb0;
+            vj0 = (r == 0) ? j : vj0;
+            vb1 = (r == 1) ? bh : vb1;
+            vj1 = (r == 1) ? j : vj1;
+            vb2 = (r == 2) ? bh : vb2;
+            vj2 = (r == 2) ? j : vj2;
+        };
+        auto issue_v = [&]() -> bool {
+            const int s = gv % L::VSTAGES;
+            const uint32_t ph = (uint32_t)(gv / L::VSTAGES) & 1u;
+            if (!warp_wait_bar(bar(L::B_VEMPTY + s), ph ^ 1u, limit, abort_flag, 0x100 + L::B_VEMPTY + s))
+                return false;
+            const int r = gv % 3;
+            const int vbh = (r == 0) ? vb0 : ((r == 1) ? vb1 : vb2);
+            const int vj = (r == 0) ? vj0 : ((r == 1) ? vj1 : vj2);
+            if (ptx::elect_one()) {
                 ptx::mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::KV_BYTES);
                 FA_TRACE_EV(8, gv, 1);
                 for (int c = 0; c < L::DBLK; ++c)
                     ptx::tma_load_3d(sbase + L::OFF_V + s * L::VSTAGE + c * BLK_BYTES, &tm_v,
-                                     bar(L::B_VFULL + s), c * 64, v_j[gv % 3] * BN, v_bh[gv % 3]);
-                ++gv;
-                return true;
-            };
-            for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
-                const Item it = item_of<CAUSAL>(i, p);
-                // Q of this item once the previous item's last score MMA is done.
-                if (!(ok = wait_bar(bar(L::B_QEMPTY), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
-                                    0x100 + L::B_QEMPTY)))
-                    break;
+                                     bar(L::B_VFULL + s), c * 64, vj * BN, vbh);
+            }
+            ++gv;
+            return true;
+        };
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const Item it = item_of<CAUSAL>(i, p);
+            // Q of this item once the previous item's last score MMA is done.
+            if (!(ok = warp_wait_bar(bar(L::B_QEMPTY), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                     0x100 + L::B_QEMPTY)))
+                break;
+            if (ptx::elect_one()) {
                 ptx::mbar_arrive_expect_tx(bar(L::B_QFULL), L::Q_BYTES);
                 for (int c = 0; c < L::DBLK; ++c)
                     ptx::tma_load_3d(sbase + L::OFF_Q + c * BLK_BYTES, &tm_q, bar(L::B_QFULL), c * 64,
                                      it.q0, it.bh);
-                for (int j = 0; ok && j < it.n_kv; ++j) {
-                    const int s = gk % L::KSTAGES;
-                    const uint32_t ph = (uint32_t)(gk / L::KSTAGES) & 1u;
-                    if (!(ok = wait_bar(bar(L::B_KEMPTY + s), ph ^ 1u, limit, abort_flag, 0x100 + L::B_KEMPTY + s)))
-                        break;
-                    if (gk == p.debug_skip_k && blockIdx.x == 0) {
-                        // Test hook: this K tile is never loaded, so the wait of
-                        // the MMA warp on it runs out (exercises the abort path).
-                        v_bh[gk % 3] = it.bh;
-                        v_j[gk % 3] = j;
-                        ++gk;
-                        if (gv <= gk - 3) ok = issue_v();
-                        continue;
-                    }
+            }
+            for (int j = 0; ok && j < it.n_kv; ++j) {
+                const int s = gk % L::KSTAGES;
+                const uint32_t ph = (uint32_t)(gk / L::KSTAGES) & 1u;
+                if (!(ok = warp_wait_bar(bar(L::B_KEMPTY + s), ph ^ 1u, limit, abort_flag,
+                                         0x100 + L::B_KEMPTY + s)))
+                    break;
+                // Test hook: a skipped K tile is never loaded, so the MMA
+                // warp's wait for it runs out (exercises the abort path).
+                const bool skip = gk == p.debug_skip_k && blockIdx.x == 0;
+                if (!skip && ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::KV_BYTES);
                     FA_TRACE_EV(8, gk, 0);
                     for (int c = 0; c < L::DBLK; ++c)
                         ptx::tma_load_3d(sbase + L::OFF_K + s * L::KV_BYTES + c * BLK_BYTES, &tm_k,
                                          bar(L::B_KFULL + s), c * 64, j * BN, it.bh);
-                    v_bh[gk % 3] = it.bh;
-                    v_j[gk % 3] = j;
-                    ++gk;
-                    if (gv <= gk - 3) ok = issue_v();
                 }
-                // The item's last V loads go out before the next item's Q: the
-                // MMA warp finishes this item (and frees Q) only with them.
-                while (ok && gv < gk) ok = issue_v();
+                remember(gk, it.bh, j);
+                ++gk;
+                if (gv <= gk - 3) ok = issue_v();
             }
-            // Drain: every copy this thread issued must land before exit.
-            if (k > 0) drain_bar(bar(L::B_QFULL), (uint32_t)((k - 1) & 1), limit, abort_flag, 0x180);
-            for (int g = max(0, gk - L::KSTAGES); g < gk; ++g)
-                if (!(g == p.debug_skip_k && blockIdx.x == 0))
-                    drain_bar(bar(L::B_KFULL + g % L::KSTAGES), (uint32_t)(g / L::KSTAGES) & 1u, limit,
-                              abort_flag, 0x181);
-            for (int g = max(0, gv - L::VSTAGES); g < gv; ++g)
-                drain_bar(bar(L::B_VFULL + g % L::VSTAGES), (uint32_t)(g / L::VSTAGES) & 1u, limit,
-                          abort_flag, 0x182);
+            // The item's last V loads go out before the next item's Q: the
+            // MMA warp finishes this item (and frees Q) only with them.
+            while (ok && gv < gk) ok = issue_v();
         }
-        // Lanes 1-31 go straight to the closing __syncthreads: parked on a
-        // CTA barrier they do not compete with lane 0 for the warp's issue.
+        // Drain: every copy this warp issued must land before exit.
+        if (k > 0) drain_bar(bar(L::B_QFULL), (uint32_t)((k - 1) & 1), limit, abort_flag, 0x180);
+        for (int g = max(0, gk - L::KSTAGES); g < gk; ++g)
+            if (!(g == p.debug_skip_k && blockIdx.x == 0))
+                drain_bar(bar(L::B_KFULL + g % L::KSTAGES), (uint32_t)(g / L::KSTAGES) & 1u, limit,
+                          abort_flag, 0x181);
+        for (int g = max(0, gv - L::VSTAGES); g < gv; ++g)
+            drain_bar(bar(L::B_VFULL + g % L::VSTAGES), (uint32_t)(g / L::VSTAGES) & 1u, limit,
+                      abort_flag, 0x182);
     } else if (warp == WARP_MMA) {
         // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
-            constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
-            // Descriptors are built once; stepping through K only moves the
-            // start-address field (bits 0-13, in 16-byte units), a plain add.
-            const uint64_t q_desc = ptx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
-            const uint64_t k_desc0 = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
-            const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
-            int g = 0, k = 0;  // tiles and items done
-            bool ok = true;
-            // S for global tile gs = Q K_j^T into S buffer (gs & 1); K-major
-            // operands, 16 columns per MMA.
-            auto issue_s = [&](int gs) -> bool {
-                const int s = gs % L::KSTAGES;
-                if (!wait_bar(bar(L::B_KFULL + s), (uint32_t)(gs / L::KSTAGES) & 1u, limit, abort_flag,
-                              0x200 + L::B_KFULL + s))
-                    return false;
-                FA_TRACE_EV(9, gs, 0);
-                ptx::tc_fence_after_sync();
-                const uint32_t d_tmem = tmem + ((gs & 1) ? TM_S1 : TM_S0);
-                const uint64_t k_desc = k_desc0 + (uint64_t)((s * L::KV_BYTES) >> 4);
+        // As for the producer: the whole warp runs the loop, one elected lane
+        // issues each MMA and commit.  A lone divergent thread would compute
+        // every descriptor on the regular datapath and lose the issue slots
+        // of its sub-partition to the softmax warps' exponent loops.
+        constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
+        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
+        // Descriptors are built once; stepping through K only moves the
+        // start-address field (bits 0-13, in 16-byte units), a plain add.
+        const uint64_t q_desc = ptx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+        const uint64_t k_desc0 = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
+        int g = 0, k = 0;  // tiles and items done
+        bool ok = true;
+        // S for global tile gs = Q K_j^T into S buffer (gs & 1); K-major
+        // operands, 16 columns per MMA.
+        auto issue_s = [&](int gs) -> bool {
+            const int s = gs % L::KSTAGES;
+            if (!warp_wait_bar(bar(L::B_KFULL + s), (uint32_t)(gs / L::KSTAGES) & 1u, limit, abort_flag,
+                               0x200 + L::B_KFULL + s))
+                return false;
+            if (lane == 0) FA_TRACE_EV(9, gs, 0);
+            ptx::tc_fence_after_sync();
+            const uint32_t d_tmem = tmem + ((gs & 1) ? TM_S1 : TM_S0);
+            const uint64_t k_desc = k_desc0 + (uint64_t)((s * L::KV_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = ((uint32_t)(kk >> 2) * BLK_BYTES + (uint32_t)(kk & 3) * 32) >> 4;
-                    ptx::mma_ss(d_tmem, q_desc + koff, k_desc + koff, IDESC_S, kk > 0 ? 1u : 0u);
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = ((uint32_t)(kk >> 2) * BLK_BYTES + (uint32_t)(kk & 3) * 32) >> 4;
+                if (ptx::elect_one()) ptx::mma_ss(d_tmem, q_desc + koff, k_desc + koff, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+            if (ptx::elect_one()) {
                 ptx::tc_commit(bar(L::B_KEMPTY + s));
                 ptx::tc_commit(bar(L::B_SFULL + (gs & 1)));
                 FA_TRACE_EV(9, gs, 1);
-                return true;
-            };
-            // [O | l~] (+)= P [V | 1] for global tile gp: A = P from TMEM (2 bf16
-            // per column, 8 columns per 16 keys, in the first half of S buffer
-            // gp & 1); B MN-major (value columns contiguous): 64-column blocks
-            // BLK_BYTES apart (the ones block follows the value blocks), 8-key
-            // groups 1024 bytes apart.
-            auto issue_pv = [&](int gp, bool first) -> bool {
-                FA_TRACE_EV(9, gp, 6);
-                const int b = gp & 1;
-                const int s = gp % L::VSTAGES;
-                if (!wait_bar(bar(L::B_PFULL + b), (uint32_t)(gp >> 1) & 1u, limit, abort_flag,
-                              0x200 + L::B_PFULL + b))
-                    return false;
-                FA_TRACE_EV(9, gp, 2);
-                if (!wait_bar(bar(L::B_VFULL + s), (uint32_t)(gp / L::VSTAGES) & 1u, limit, abort_flag,
-                              0x200 + L::B_VFULL + s))
-                    return false;
-                FA_TRACE_EV(9, gp, 3);
-                ptx::tc_fence_after_sync();
-                const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
-                const uint32_t p_tmem = tmem + (b ? TM_S1 : TM_S0);
+            }
+            return true;
+        };
+        // [O | l~] (+)= P [V | 1] for global tile gp: A = P from TMEM (2 bf16
+        // per column, 8 columns per 16 keys, in the first half of S buffer
+        // gp & 1); B MN-major (value columns contiguous): 64-column blocks
+        // BLK_BYTES apart (the ones block follows the value blocks), 8-key
+        // groups 1024 bytes apart.
+        auto issue_pv = [&](int gp, bool first) -> bool {
+            if (lane == 0) FA_TRACE_EV(9, gp, 6);
+            const int b = gp & 1;
+            const int s = gp % L::VSTAGES;
+            if (!warp_wait_bar(bar(L::B_PFULL + b), (uint32_t)(gp >> 1) & 1u, limit, abort_flag,
+                               0x200 + L::B_PFULL + b))
+                return false;
+            if (lane == 0) FA_TRACE_EV(9, gp, 2);
+            if (!warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(gp / L::VSTAGES) & 1u, limit, abort_flag,
+                               0x200 + L::B_VFULL + s))
+                return false;
+            if (lane == 0) FA_TRACE_EV(9, gp, 3);
+            ptx::tc_fence_after_sync();
+            const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
+            const uint32_t p_tmem = tmem + (b ? TM_S1 : TM_S0);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                if (ptx::elect_one())
                     ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
                                 v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
                                 (!first || kk > 0) ? 1u : 0u);
-                    if (kk == 0) FA_TRACE_EV(9, gp, 5);
-                    if (kk == 7) FA_TRACE_EV(9, gp, 7);
-                }
+                if (kk == 0 && lane == 0) FA_TRACE_EV(9, gp, 5);
+                if (kk == 7 && lane == 0) FA_TRACE_EV(9, gp, 7);
+            }
+            if (ptx::elect_one()) {
                 ptx::tc_commit(bar(L::B_VEMPTY + s));
                 ptx::tc_commit(bar(L::B_ODONE));
                 FA_TRACE_EV(9, gp, 4);
-                return true;
-            };
-            for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
-                const int n = item_of<CAUSAL>(i, p).n_kv;
-                if (!(ok = wait_bar(bar(L::B_QFULL), (uint32_t)(k & 1), limit, abort_flag, 0x200 + L::B_QFULL)))
-                    break;
-                ptx::tc_fence_after_sync();
-                // The first two score tiles run while the softmax warps finish
-                // the previous item.
-                if (!(ok = issue_s(g))) break;
-                if (n > 1 && !(ok = issue_s(g + 1))) break;
-                if (n <= 2) ptx::tc_commit(bar(L::B_QEMPTY));
-                // The first P.V of an item overwrites O: wait until the softmax
-                // warps have read out the previous item's O.
-                if (!(ok = wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
-                                    0x200 + L::B_OFREE)))
-                    break;
-                for (int j = 0; ok && j < n; ++j) {
-                    if (!(ok = issue_pv(g + j, j == 0))) break;
-                    if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
-                    // S two tiles ahead reuses buffer (g + j) & 1, after P V read it.
-                    if (j + 2 < n) {
-                        if (!(ok = issue_s(g + j + 2))) break;
-                        if (j + 3 == n) ptx::tc_commit(bar(L::B_QEMPTY));
-                    }
-                }
-                g += n;
             }
-            // Drain: all MMAs issued by this thread complete before TMEM is freed.
-            ptx::tc_commit(bar(L::B_DRAIN));
-            drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
+            return true;
+        };
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const int n = item_of<CAUSAL>(i, p).n_kv;
+            if (!(ok = warp_wait_bar(bar(L::B_QFULL), (uint32_t)(k & 1), limit, abort_flag, 0x200 + L::B_QFULL)))
+                break;
+            ptx::tc_fence_after_sync();
+            // The first two score tiles run while the softmax warps finish
+            // the previous item.
+            if (!(ok = issue_s(g))) break;
+            if (n > 1 && !(ok = issue_s(g + 1))) break;
+            if (n <= 2 && ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY));
+            // The first P.V of an item overwrites O: wait until the softmax
+            // warps have read out the previous item's O.
+            if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                     0x200 + L::B_OFREE)))
+                break;
+            for (int j = 0; ok && j < n; ++j) {
+                if (!(ok = issue_pv(g + j, j == 0))) break;
+                if (j == n - 1 && ptx::elect_one()) ptx::tc_commit(bar(L::B_OFINAL));
+                // S two tiles ahead reuses buffer (g + j) & 1, after P V read it.
+                if (j + 2 < n) {
+                    if (!(ok = issue_s(g + j + 2))) break;
+                    if (j + 3 == n && ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY));
+                }
+            }
+            g += n;
         }
+        // Drain: all MMAs issued by this warp complete before TMEM is freed.
+        if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
+        drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
     } else {
         // ---------------------------------------------------- softmax warps
         const int quarter = warp & 3;
