@@ -21,7 +21,7 @@
 // items: the next item's Q load and first score MMAs overlap the current
 // item's last tiles and epilogue.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-7  softmax.  Warp w serves query rows 32*(w%4) .. +31 (its TMEM
 //              lane quarter) and score columns 64*(w/4) .. +63, so every SM
 //              sub-partition runs two softmax warps (w and w+4, the two halves
@@ -32,17 +32,22 @@
 //              those columns (straight from registers to global memory).
 //   warp 8     TMA producer: Q once per item, K_j / V_j into rings of stages,
 //              K two tiles ahead of V.
-//   warp 9     MMA issuer (one thread), also allocates TMEM.
+//   warp 9     score MMA issuer (S_j = Q K_j^T); also allocates TMEM.
+//   warp 10    P.V MMA issuer.
+//   The three are converged warps; one elected lane issues each copy, MMA
+//   and commit.  Two MMA issuers on two sub-partitions halve the instruction
+//   stream each must get through per tile while the softmax warps' exponent
+//   loops take most of the issue slots.
 //
 // TMEM columns (512 allocated, lanes = query rows):
 //   [  0,128) S buffer 0     [128,256) S buffer 1   (fp32 scores, double-buffered)
 //   [256,256+d) O (fp32)     [256+d, 256+d+16) l~ (16 equal copies)
-//   [400,402) the two halves' fp32 row sums, exchanged in the epilogue
-// P_j (bf16 pairs, 64 columns) is written over the first half of S_j's buffer
-// once both halves of every row have read their scores.  The MMA warp issues
-// P_j V_j as soon as P_j is written and then S_{j+2} into the same buffer; the
-// tensor pipe executes one thread's MMAs in issue order, so S_{j+2} cannot
-// overwrite P_j before P_j V_j has read it.
+//   [400,464) P (bf16 pairs, one tile)
+//   [464,466) the two halves' fp32 row sums, exchanged in the epilogue
+// S_{j+2} goes into S_j's buffer as soon as every softmax warp has read S_j
+// into registers (S_READ); P_j goes into the P buffer once P_{j-1} V_{j-1} is
+// complete (O_DONE).  So the score stream runs ahead of the P.V stream and
+// neither issuer waits for the other.
 //
 // l~ = rowsum(bf16(P)): each V stage carries a 64-wide block of ones after
 // its d value columns, and the P.V MMA runs with N = d + 16, so the tensor
@@ -70,12 +75,13 @@ constexpr int BM = 128;  // query rows per work item
 constexpr int BN = 128;  // keys per K/V tile
 constexpr int SOFTMAX_THREADS = 256;
 constexpr int SOFTMAX_WARPS = SOFTMAX_THREADS / 32;
-constexpr int NUM_THREADS = SOFTMAX_THREADS + 64;
+constexpr int NUM_THREADS = SOFTMAX_THREADS + 96;
 constexpr int WARP_TMA = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA_S = 9;
+constexpr int WARP_MMA_O = 10;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t WAIT_SLEEP_NS = 20000;  // suspend-time hint of one poll
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_LX = 400;
+constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P = 400, TM_LX = 464;
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t BLK_BYTES = BN * 128;  // one 64-column, 128-row swizzled block (16 KB)
 
@@ -104,7 +110,7 @@ struct Layout {
     static constexpr int VSTAGES = (D == 128) ? 2 : 4;
     static constexpr int DBLK = D / 64;                   // 64-column blocks of a row
     static constexpr uint32_t TM_L = TM_O + D;            // l~ columns
-    static_assert(TM_L + 16 <= TM_LX && TM_LX + 2 <= TM_COLS, "TMEM budget");
+    static_assert(TM_L + 16 <= TM_P && TM_P + 64 <= TM_LX && TM_LX + 2 <= TM_COLS, "TMEM budget");
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;      // bytes of one K or V tile
     static constexpr uint32_t VSTAGE = (DBLK + 1) * BLK_BYTES;  // V blocks + the ones block
@@ -120,13 +126,14 @@ struct Layout {
     static constexpr int B_KEMPTY = B_KFULL + KSTAGES;
     static constexpr int B_VFULL = B_KEMPTY + KSTAGES;
     static constexpr int B_VEMPTY = B_VFULL + VSTAGES;
-    static constexpr int B_SFULL = B_VEMPTY + VSTAGES;  // 2 (per S buffer)
-    static constexpr int B_PFULL = B_SFULL + 2;         // 2 (per S buffer)
-    static constexpr int B_ODONE = B_PFULL + 2;  // every P.V
+    static constexpr int B_SFULL = B_VEMPTY + VSTAGES;  // 2 (per S buffer): S written
+    static constexpr int B_SREAD = B_SFULL + 2;         // 2 (per S buffer): S read out
+    static constexpr int B_PFULL = B_SREAD + 2;         // P written
+    static constexpr int B_ODONE = B_PFULL + 1;  // every P.V
     static constexpr int B_OFINAL = B_ODONE + 1; // the last P.V of an item
     static constexpr int B_OFREE = B_OFINAL + 1;
-    static constexpr int B_DRAIN = B_OFREE + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_OFREE + 1;  // 2 (one per MMA issuer)
+    static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort
     // The dynamic shared memory base is 1024-byte aligned (no static shared
     // memory); the kernel checks it and refuses to run otherwise.
@@ -140,10 +147,10 @@ __device__ unsigned int g_status_where;  // first wait code that gave up (+1)
 // Optional event trace for pipeline studies (compiled only with FA_TRACE):
 // clock64() stamps of selected events of the first TRACE_CTAS CTAs, written to
 // g_trace[cta][role][tile * 8 + event] for tiles < TRACE_TILES; role = warp
-// index (softmax warps 0-7, producer 8, MMA issuer 9); tile counts all tiles
+// index (softmax warps 0-7, producer 8, MMA issuers 9 and 10); tile counts all tiles
 // the CTA processed so far.
 #ifdef FA_TRACE
-constexpr int TRACE_CTAS = 8, TRACE_ROLES = 10, TRACE_TILES = 64;
+constexpr int TRACE_CTAS = 8, TRACE_ROLES = 11, TRACE_TILES = 64;
 __device__ unsigned long long* g_trace;
 #define FA_TRACE_EV(role, tile, ev)                                                                  \
     do {                                                                                             \
@@ -169,7 +176,7 @@ __device__ __forceinline__ void record_timeout(uint32_t code, volatile uint32_t*
 // abort flag and the clock are looked at only every 256 polls.  A waiting
 // thread sleeps in try_wait (woken when the phase completes) rather than
 // spinning: a spinning warp takes issue slots from the warps on its SM
-// sub-partition, among them the single thread that issues the MMAs.
+// sub-partition, among them the MMA issuers.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint64_t limit_ns,
                                          volatile uint32_t* abort_flag, uint32_t code)
 {
@@ -315,12 +322,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Softmax-side barriers count warps: each warp arrives once, after __syncwarp.
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(L::B_SFULL + b), 1);
-            ptx::mbar_init(bar(L::B_PFULL + b), SOFTMAX_WARPS);
+            ptx::mbar_init(bar(L::B_SREAD + b), SOFTMAX_WARPS);
         }
+        ptx::mbar_init(bar(L::B_PFULL), SOFTMAX_WARPS);
         ptx::mbar_init(bar(L::B_ODONE), 1);
         ptx::mbar_init(bar(L::B_OFINAL), 1);
         ptx::mbar_init(bar(L::B_OFREE), SOFTMAX_WARPS);
         ptx::mbar_init(bar(L::B_DRAIN), 1);
+        ptx::mbar_init(bar(L::B_DRAIN + 1), 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
     }
@@ -340,7 +349,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
     }
-    if (warp == WARP_MMA) {
+    if (warp == WARP_MMA_S) {
         ptx::tmem_alloc(sbase + L::OFF_MISC, TM_COLS);
         ptx::tmem_relinquish();
     }
@@ -432,109 +441,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int g = max(0, gv - L::VSTAGES); g < gv; ++g)
             drain_bar(bar(L::B_VFULL + g % L::VSTAGES), (uint32_t)(g / L::VSTAGES) & 1u, limit,
                       abort_flag, 0x182);
-    } else if (warp == WARP_MMA) {
-        // -------------------------------------------------------- MMA issuer
-        // As for the producer: the whole warp runs the loop, one elected lane
-        // issues each MMA and commit.  A lone divergent thread would compute
-        // every descriptor on the regular datapath and lose the issue slots
-        // of its sub-partition to the softmax warps' exponent loops.
+    } else if (warp == WARP_MMA_S) {
+        // ------------------------------------------------- score MMA issuer
+        // S for global tile g = Q K_j^T into S buffer g & 1; K-major operands,
+        // 16 columns per MMA.  Descriptors are built once; stepping through K
+        // only moves the start-address field (bits 0-13, in 16-byte units).
         constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
-        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
-        // Descriptors are built once; stepping through K only moves the
-        // start-address field (bits 0-13, in 16-byte units), a plain add.
         const uint64_t q_desc = ptx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
         const uint64_t k_desc0 = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
-        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
         int g = 0, k = 0;  // tiles and items done
         bool ok = true;
-        // S for global tile gs = Q K_j^T into S buffer (gs & 1); K-major
-        // operands, 16 columns per MMA.
-        auto issue_s = [&](int gs) -> bool {
-            const int s = gs % L::KSTAGES;
-            if (!warp_wait_bar(bar(L::B_KFULL + s), (uint32_t)(gs / L::KSTAGES) & 1u, limit, abort_flag,
-                               0x200 + L::B_KFULL + s))
-                return false;
-            if (lane == 0) FA_TRACE_EV(9, gs, 0);
-            ptx::tc_fence_after_sync();
-            const uint32_t d_tmem = tmem + ((gs & 1) ? TM_S1 : TM_S0);
-            const uint64_t k_desc = k_desc0 + (uint64_t)((s * L::KV_BYTES) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t koff = ((uint32_t)(kk >> 2) * BLK_BYTES + (uint32_t)(kk & 3) * 32) >> 4;
-                if (ptx::elect_one()) ptx::mma_ss(d_tmem, q_desc + koff, k_desc + koff, IDESC_S, kk > 0 ? 1u : 0u);
-            }
-            if (ptx::elect_one()) {
-                ptx::tc_commit(bar(L::B_KEMPTY + s));
-                ptx::tc_commit(bar(L::B_SFULL + (gs & 1)));
-                FA_TRACE_EV(9, gs, 1);
-            }
-            return true;
-        };
-        // [O | l~] (+)= P [V | 1] for global tile gp: A = P from TMEM (2 bf16
-        // per column, 8 columns per 16 keys, in the first half of S buffer
-        // gp & 1); B MN-major (value columns contiguous): 64-column blocks
-        // BLK_BYTES apart (the ones block follows the value blocks), 8-key
-        // groups 1024 bytes apart.
-        auto issue_pv = [&](int gp, bool first) -> bool {
-            if (lane == 0) FA_TRACE_EV(9, gp, 6);
-            const int b = gp & 1;
-            const int s = gp % L::VSTAGES;
-            if (!warp_wait_bar(bar(L::B_PFULL + b), (uint32_t)(gp >> 1) & 1u, limit, abort_flag,
-                               0x200 + L::B_PFULL + b))
-                return false;
-            if (lane == 0) FA_TRACE_EV(9, gp, 2);
-            if (!warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(gp / L::VSTAGES) & 1u, limit, abort_flag,
-                               0x200 + L::B_VFULL + s))
-                return false;
-            if (lane == 0) FA_TRACE_EV(9, gp, 3);
-            ptx::tc_fence_after_sync();
-            const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
-            const uint32_t p_tmem = tmem + (b ? TM_S1 : TM_S0);
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                if (ptx::elect_one())
-                    ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
-                                v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
-                                (!first || kk > 0) ? 1u : 0u);
-                if (kk == 0 && lane == 0) FA_TRACE_EV(9, gp, 5);
-                if (kk == 7 && lane == 0) FA_TRACE_EV(9, gp, 7);
-            }
-            if (ptx::elect_one()) {
-                ptx::tc_commit(bar(L::B_VEMPTY + s));
-                ptx::tc_commit(bar(L::B_ODONE));
-                FA_TRACE_EV(9, gp, 4);
-            }
-            return true;
-        };
         for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
             const int n = item_of<CAUSAL>(i, p).n_kv;
             if (!(ok = warp_wait_bar(bar(L::B_QFULL), (uint32_t)(k & 1), limit, abort_flag, 0x200 + L::B_QFULL)))
                 break;
-            ptx::tc_fence_after_sync();
-            // The first two score tiles run while the softmax warps finish
-            // the previous item.
-            if (!(ok = issue_s(g))) break;
-            if (n > 1 && !(ok = issue_s(g + 1))) break;
-            if (n <= 2 && ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY));
+            for (int j = 0; j < n; ++j, ++g) {
+                const int b = g & 1;
+                const int s = g % L::KSTAGES;
+                // Buffer b is free once every softmax warp has read S of tile
+                // g - 2 (the phase before cannot alias: S of g - 2 was issued
+                // only after S of g - 4 had been read).
+                if (g >= 2 && !(ok = warp_wait_bar(bar(L::B_SREAD + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
+                                                   abort_flag, 0x200 + L::B_SREAD + b)))
+                    break;
+                if (!(ok = warp_wait_bar(bar(L::B_KFULL + s), (uint32_t)(g / L::KSTAGES) & 1u, limit,
+                                         abort_flag, 0x200 + L::B_KFULL + s)))
+                    break;
+                if (lane == 0) FA_TRACE_EV(9, g, 0);
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem + (b ? TM_S1 : TM_S0);
+                const uint64_t k_desc = k_desc0 + (uint64_t)((s * L::KV_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = ((uint32_t)(kk >> 2) * BLK_BYTES + (uint32_t)(kk & 3) * 32) >> 4;
+                    if (ptx::elect_one())
+                        ptx::mma_ss(d_tmem, q_desc + koff, k_desc + koff, IDESC_S, kk > 0 ? 1u : 0u);
+                }
+                if (ptx::elect_one()) {
+                    ptx::tc_commit(bar(L::B_KEMPTY + s));
+                    ptx::tc_commit(bar(L::B_SFULL + b));
+                    // Q may be replaced once the item's last score MMA is done.
+                    if (j == n - 1) ptx::tc_commit(bar(L::B_QEMPTY));
+                    FA_TRACE_EV(9, g, 1);
+                }
+            }
+        }
+        // Drain: all MMAs issued by this warp complete before TMEM is freed.
+        if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
+        drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
+    } else if (warp == WARP_MMA_O) {
+        // ------------------------------------------------- P.V MMA issuer
+        // [O | l~] (+)= P [V | 1] for global tile g: A = P from TMEM (2 bf16
+        // per column, 8 columns per 16 keys); B MN-major (value columns
+        // contiguous): 64-column blocks BLK_BYTES apart (the ones block follows
+        // the value blocks), 8-key groups 1024 bytes apart.
+        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
+        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
+        const uint32_t p_tmem = tmem + TM_P;
+        int g = 0, k = 0;  // tiles and items done
+        bool ok = true;
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const int n = item_of<CAUSAL>(i, p).n_kv;
             // The first P.V of an item overwrites O: wait until the softmax
             // warps have read out the previous item's O.
             if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
                                      0x200 + L::B_OFREE)))
                 break;
-            for (int j = 0; ok && j < n; ++j) {
-                if (!(ok = issue_pv(g + j, j == 0))) break;
-                if (j == n - 1 && ptx::elect_one()) ptx::tc_commit(bar(L::B_OFINAL));
-                // S two tiles ahead reuses buffer (g + j) & 1, after P V read it.
-                if (j + 2 < n) {
-                    if (!(ok = issue_s(g + j + 2))) break;
-                    if (j + 3 == n && ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY));
+            for (int j = 0; j < n; ++j, ++g) {
+                const int s = g % L::VSTAGES;
+                // P of tile g (the phase before is P of g - 1, which this warp
+                // has consumed, so parity cannot alias).
+                if (!(ok = warp_wait_bar(bar(L::B_PFULL), (uint32_t)(g & 1), limit, abort_flag,
+                                         0x200 + L::B_PFULL)))
+                    break;
+                if (lane == 0) FA_TRACE_EV(10, g, 2);
+                if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
+                                         abort_flag, 0x200 + L::B_VFULL + s)))
+                    break;
+                if (lane == 0) FA_TRACE_EV(10, g, 3);
+                ptx::tc_fence_after_sync();
+                const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (ptx::elect_one())
+                        ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
+                                    v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    if (kk == 0 && lane == 0) FA_TRACE_EV(10, g, 5);
+                    if (kk == 7 && lane == 0) FA_TRACE_EV(10, g, 7);
+                }
+                if (ptx::elect_one()) {
+                    ptx::tc_commit(bar(L::B_VEMPTY + s));
+                    ptx::tc_commit(bar(L::B_ODONE));
+                    if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
+                    FA_TRACE_EV(10, g, 4);
                 }
             }
-            g += n;
         }
-        // Drain: all MMAs issued by this warp complete before TMEM is freed.
-        if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
-        drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
+        if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN + 1));
+        drain_bar(bar(L::B_DRAIN + 1), 0, limit, abort_flag, 0x281);
     } else {
         // ---------------------------------------------------- softmax warps
         const int quarter = warp & 3;
@@ -583,6 +588,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         s[c] = __uint_as_float(r0[c]);
                         s[32 + c] = __uint_as_float(r1[c]);
                     }
+                    // The scores are in registers: S of tile g + 2 may now be
+                    // written into this buffer.
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(L::B_SREAD + b));
                     if (lane == 0) FA_TRACE_EV(warp, g, 1);
                     // Causal diagonal tile / keys past N: -inf before the max.
                     const int k0 = j * BN + half * 64;
@@ -601,6 +611,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * BM + row]);
                 const float m_tile = mx * sl2;  // scale > 0, so max commutes with it
 
+                // [O | l~] and the P buffer are free of tile g - 1 once its P.V
+                // is done (O_DONE; the phase before, P.V of g - 2, was waited
+                // for before P of g - 1 was written, so parity cannot alias).
+                bool o_done = g == 0;
+                auto wait_o_done = [&]() -> bool {
+                    if (o_done) return true;
+                    if (!warp_wait_bar(bar(L::B_ODONE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
+                                       0x300 + L::B_ODONE))
+                        return false;
+                    ptx::tc_fence_after_sync();
+                    o_done = true;
+                    return true;
+                };
                 if (j == 0) {
                     m_ref = (m_tile == -INFINITY) ? 0.f : m_tile;
                 } else {
@@ -608,15 +631,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const bool need = m_new > m_ref + RESCALE_LOG2;
                     // Both halves of a row see the same values, so they decide alike.
                     if (__any_sync(0xffffffffu, need)) {
-                        // [O | l~] hold everything up to the previous tile once its
-                        // P.V is done.  The P.V before that is complete (S of this
-                        // tile was issued after it; for the second tile of an item,
-                        // the epilogue of the previous item waited for it), so the
-                        // parity wait cannot be fooled.
-                        ok = warp_wait_bar(bar(L::B_ODONE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
-                                           0x300 + L::B_ODONE);
-                        if (!ok) continue;
-                        ptx::tc_fence_after_sync();
+                        // [O | l~] hold everything up to the previous tile once
+                        // its P.V is done.
+                        if (!(ok = wait_o_done())) continue;
                         const float corr = ptx::ex2(m_ref - m_new);
 #pragma unroll
                         for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
@@ -651,13 +668,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (lane == 0) FA_TRACE_EV(warp, g, 3);
 
-                // P over the first half of S buffer b (both halves of each row
-                // read their scores before the pair barrier above).
-                ptx::tmem_st32(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 32, pk);
+                // P into the P buffer once the previous tile's P.V has read it.
+                if (!(ok = wait_o_done())) continue;
+                ptx::tmem_st32(tmem + lane_off + TM_P + (uint32_t)half * 32, pk);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + b));
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL));
                 if (lane == 0) FA_TRACE_EV(warp, g, 5);
             }
 
@@ -721,7 +738,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     ptx::tc_fence_before_sync();
     __syncthreads();
-    if (warp == WARP_MMA) {
+    if (warp == WARP_MMA_S) {
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, TM_COLS);
     }
