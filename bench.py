@@ -99,6 +99,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank value over the default process group; the value itself
+    when no group is initialised.  The reduction tensor lives on `device` (the
+    rank's GPU under NCCL, the CPU under gloo)."""
+    import torch
+    import torch.distributed as distm
+
+    if not (distm.is_available() and distm.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    distm.all_reduce(t, op=distm.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own copy of the workload (weak
+    scaling), timed by the slowest rank."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -278,10 +298,7 @@ def main(argv=None):
     ms = ev0.elapsed_time(ev1)
     if fa.check_device_status() != 0:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        distm.all_reduce(t, op=distm.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_per_step = ms / args.steps
 
     # Spread of single launches (each bracketed by its own events), after the
@@ -299,7 +316,7 @@ def main(argv=None):
     launch_stats = {"n": len(single_ms), "median_ms": round(statistics.median(single_ms), 5),
                     "stdev_ms": round(statistics.stdev(single_ms), 5),
                     "min_ms": round(min(single_ms), 5)}
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = job_tflops(flops, world, ms_per_step)
 
     # ---- end to end through the public call with host buffers
     e2e = None
@@ -330,14 +347,10 @@ def main(argv=None):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = e0.elapsed_time(e1)
-        if pg:
-            t = torch.tensor([ems], device=dev)
-            distm.all_reduce(t, op=distm.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": flops * world / (ems / n_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(flops, world, ems / n_e2e), "unit": "TFLOP/s",
                "ms_per_step": ems / n_e2e, "steps": n_e2e, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
