@@ -224,13 +224,14 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, uin
     return __all_sync(0xffffffffu, ok);
 }
 
-// Max of 64 values with 3-input max instructions (depth 4).
-__device__ __forceinline__ float max64(const float (&s)[64])
+// Max of 64 values (fp32 bit patterns) with 3-input max instructions (depth 4).
+__device__ __forceinline__ float max64(const uint32_t (&s)[64])
 {
     float t[22];
 #pragma unroll
-    for (int i = 0; i < 21; ++i) t[i] = ptx::fmax3(s[3 * i], s[3 * i + 1], s[3 * i + 2]);
-    t[21] = s[63];
+    for (int i = 0; i < 21; ++i)
+        t[i] = ptx::fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]), __uint_as_float(s[3 * i + 2]));
+    t[21] = __uint_as_float(s[63]);
     float u[8];
 #pragma unroll
     for (int i = 0; i < 7; ++i) u[i] = ptx::fmax3(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
@@ -565,29 +566,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float m_ref = -INFINITY;
             // This half-row's sum of probabilities, as four packed fp32 pairs.
             uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+            {
+            // This half-row's scores (fp32 bit patterns), used in place: the
+            // packed fp32x2 arithmetic takes neighbouring load registers as
+            // its operand pairs.
+            uint32_t sr[64];
 
             for (int j = 0; j < it.n_kv; ++j, ++g) {
                 const int b = g & 1;
                 if (ok) {
                     ok = warp_wait_bar(bar(L::B_SFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
                                        0x300 + L::B_SFULL + b);
+                    if (ok) {
+                        ptx::tc_fence_after_sync();
+                        ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
+                    }
                 }
                 if (lane == 0) FA_TRACE_EV(warp, g, 0);
-                float s[64];
                 float mx = -INFINITY;
                 if (ok) {
-                    ptx::tc_fence_after_sync();
-                    uint32_t r0[32], r1[32];
-                    const uint32_t s_tmem = tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64;
-                    ptx::tmem_ld32(s_tmem + 0, r0);
-                    ptx::tmem_ld32(s_tmem + 32, r1);
-                    ptx::tmem_wait_ld(r0);
-                    ptx::reg_fence(r1);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        s[c] = __uint_as_float(r0[c]);
-                        s[32 + c] = __uint_as_float(r1[c]);
-                    }
+                    ptx::tmem_wait_ld64(sr);
                     // The scores are in registers: S of tile g + 2 may now be
                     // written into this buffer.
                     ptx::tc_fence_before_sync();
@@ -599,9 +597,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (j * BN + BN - 1 > cta_key_max) {
 #pragma unroll
                         for (int c = 0; c < 64; ++c)
-                            if (k0 + c > key_max) s[c] = -INFINITY;
+                            if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
                     }
-                    mx = max64(s);
+                    mx = max64(sr);
                     red[(b * 2 + half) * BM + row] = mx;
                 }
                 // Row max: this half's, then the partner warp's through shared memory.
@@ -660,7 +658,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     float x0, x1;
-                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2), x0, x1);
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                               sl2x2, neg_m2),
+                                   x0, x1);
                     const float a0 = ptx::ex2(x0);
                     const float a1 = ptx::ex2(x1);
                     lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
@@ -676,6 +676,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL));
                 if (lane == 0) FA_TRACE_EV(warp, g, 5);
+            }
             }
 
             // --------------------------------------------------- epilogue
