@@ -52,7 +52,8 @@ KERNEL_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
 # is scaled by 4 to a full launch: every (batch, head) problem moves the same
 # bytes.  profiles/ holds the summary and the command.
 MEASURED_TRAFFIC = {
-    "b8_h32_n4096_d128_causal": {"sha256": "f87278cd263f5b21697b976a8e9736222b9006f6aae2d0f78c39e759ee965dd6", "bytes": 4 * (201_518_336 + 45_228_032),
+    "b8_h32_n4096_d128_causal": {"sha256": "bb5f09a86de176ede95ba6d6d881fd6ca60c5fd29f8847477cc260fe0f631eda",
+                                 "bytes": 4 * (201_426_432 + 45_347_584),
                                  "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
