@@ -84,8 +84,11 @@ class Oracle:
         lib.oracle_attn_rows_f64.argtypes = head + [i64p, i64p, i64, f64p, f64p, c_int]
         lib.oracle_attn_online_f64.argtypes = head + [i64, f64p, f64p, c_int]
         lib.oracle_max_threads.argtypes = []
+        rect = [u16p, u16p, u16p, i64, i64, i64, i64, i64, c_int, c_dbl]
+        lib.oracle_attn_rect_f64.argtypes = rect + [f64p, f64p, c_int]
+        lib.oracle_attn_rect_rows_f64.argtypes = rect + [i64p, i64p, i64, f64p, f64p, c_int]
         for fn in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_online_f64,
-                   lib.oracle_max_threads):
+                   lib.oracle_max_threads, lib.oracle_attn_rect_f64, lib.oracle_attn_rect_rows_f64):
             fn.restype = c_int
         self.lib = lib
 
@@ -161,6 +164,54 @@ class Oracle:
         return o, lse
 
 
+    def attention_rect(self, q, k, v, causal: bool, scale: float, threads: int = 0):
+        """Decode attention: q (B, H, Nq, d) against k, v (B, H, Nk, d); query i
+        stands at key position Nk - Nq + i (the causal window ends there).
+
+        Returns ``(o (B, H, Nq, d), lse (B, H, Nq))`` float64.
+        """
+        qb, kb, vb = _bits(q), _bits(k), _bits(v)
+        B, H, Nq, d, Nk = _shape_rect(qb, kb, vb)
+        o = np.empty((B, H, Nq, d), np.float64)
+        lse = np.empty((B, H, Nq), np.float64)
+        rc = self.lib.oracle_attn_rect_f64(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                           _ptr(vb, ctypes.c_uint16), B, H, Nq, Nk, d,
+                                           int(bool(causal)), float(scale), _ptr(o, ctypes.c_double),
+                                           _ptr(lse, ctypes.c_double), int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attn_rect_f64 failed ({rc})")
+        return o, lse
+
+    def attention_rect_rows(self, q, k, v, causal: bool, scale: float, bh_idx, row_idx,
+                            threads: int = 0):
+        """Selected rows of :meth:`attention_rect` (query ``row_idx[t]`` of
+        flattened head ``bh_idx[t]``)."""
+        qb, kb, vb = _bits(q), _bits(k), _bits(v)
+        B, H, Nq, d, Nk = _shape_rect(qb, kb, vb)
+        bh = np.ascontiguousarray(np.asarray(bh_idx, dtype=np.int64))
+        rows = np.ascontiguousarray(np.asarray(row_idx, dtype=np.int64))
+        if bh.shape != rows.shape or bh.ndim != 1:
+            raise ValueError("bh_idx and row_idx must be 1-D and of equal length")
+        n = int(bh.shape[0])
+        o = np.empty((n, d), np.float64)
+        lse = np.empty((n,), np.float64)
+        rc = self.lib.oracle_attn_rect_rows_f64(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                                _ptr(vb, ctypes.c_uint16), B, H, Nq, Nk, d,
+                                                int(bool(causal)), float(scale), _ptr(bh, ctypes.c_int64),
+                                                _ptr(rows, ctypes.c_int64), n, _ptr(o, ctypes.c_double),
+                                                _ptr(lse, ctypes.c_double), int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attn_rect_rows_f64 failed ({rc})")
+        return o, lse
+
+
+def _shape_rect(q, k, v):
+    if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError(f"q (B, H, Nq, d) and k, v (B, H, Nk, d) expected: {q.shape} {k.shape} {v.shape}")
+    B, H, Nq, d = (int(s) for s in q.shape)
+    return B, H, Nq, d, int(k.shape[2])
+
+
 _default = None
 
 
@@ -196,3 +247,11 @@ def bf16_to_f64(x) -> np.ndarray:
     """Exact widening of bf16 values (tensor or bits) to float64."""
     b = _bits(x).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+def attention_rect(q, k, v, causal, scale, threads=0):
+    return _oracle().attention_rect(q, k, v, causal, scale, threads)
+
+
+def attention_rect_rows(q, k, v, causal, scale, bh_idx, row_idx, threads=0):
+    return _oracle().attention_rect_rows(q, k, v, causal, scale, bh_idx, row_idx, threads)

@@ -237,6 +237,113 @@ int oracle_attn_online_f64(const uint16_t *q, const uint16_t *k, const uint16_t 
     return failed ? -2 : 0;
 }
 
+/* ------------------------------------------------------------------------
+ * Rectangular attention (decode): Nq query rows against a cache of Nk keys.
+ * Query i stands at key position Nk - Nq + i (the newest Nq keys belong to
+ * the queries), so under the causal mask it sees keys 0 .. Nk - Nq + i;
+ * without the mask it sees all Nk.  For one query (the decode step of
+ * "Fusion and IO-aware kernels", section "Where it breaks": one query token
+ * per sequence, reading the whole KV cache) both are the same.  Each row is
+ * the same definition as above: scores, mask, two-pass softmax, P.V,
+ * logsumexp.  q, o: (B, H, Nq, d); k, v: (B, H, Nk, d); lse: (B, H, Nq).
+ * ------------------------------------------------------------------------ */
+static void attention_row_keys(const uint16_t *q_row, const uint16_t *k, const uint16_t *v,
+                               int64_t Nk, int64_t d, int64_t last_key, double scale,
+                               double *s_row, double *o_row, double *lse)
+{
+    for (int64_t j = 0; j < Nk; ++j) {
+        if (j > last_key) {
+            s_row[j] = -INFINITY;
+            continue;
+        }
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += bf16_bits_to_f64(q_row[c]) * bf16_bits_to_f64(k[j * d + c]);
+        s_row[j] = acc * scale;
+    }
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Nk; ++j)
+        if (s_row[j] > m) m = s_row[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        const double e = exp(s_row[j] - m);
+        s_row[j] = e;
+        l += e;
+    }
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (int64_t j = 0; j < Nk; ++j) {
+        const double pj = s_row[j] / l;
+        if (pj == 0.0) continue;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += pj * bf16_bits_to_f64(v[j * d + c]);
+    }
+    *lse = log(l) + m;
+}
+
+static int bad_rect(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal)
+{
+    return B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || (causal && Nq > Nk);
+}
+
+/* Full tensor.  o: B*H*Nq*d doubles, lse: B*H*Nq doubles. */
+int oracle_attn_rect_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v, int64_t B,
+                         int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, double scale,
+                         double *o, double *lse, int nthreads)
+{
+    if (!q || !k || !v || !o || !lse || bad_rect(B, H, Nq, Nk, d, causal)) return -1;
+    const int64_t rows = B * H * Nq;
+    int failed = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads))
+    {
+        double *s_row = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s_row) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!s_row) continue;
+            const int64_t bh = r / Nq, i = r % Nq;
+            const int64_t last = causal ? Nk - Nq + i : Nk - 1;
+            attention_row_keys(q + r * d, k + bh * Nk * d, v + bh * Nk * d, Nk, d, last, scale,
+                               s_row, o + r * d, lse + r);
+        }
+        free(s_row);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Selected rows: row t is query row_idx[t] of flattened head bh_idx[t]. */
+int oracle_attn_rect_rows_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                              double scale, const int64_t *bh_idx, const int64_t *row_idx,
+                              int64_t nrows, double *o_rows, double *lse_rows, int nthreads)
+{
+    if (!q || !k || !v || !bh_idx || !row_idx || !o_rows || !lse_rows || nrows < 0 ||
+        bad_rect(B, H, Nq, Nk, d, causal))
+        return -1;
+    for (int64_t t = 0; t < nrows; ++t)
+        if (bh_idx[t] < 0 || bh_idx[t] >= B * H || row_idx[t] < 0 || row_idx[t] >= Nq) return -1;
+    int failed = 0;
+#pragma omp parallel num_threads(pick_threads(nthreads))
+    {
+        double *s_row = (double *)malloc((size_t)Nk * sizeof(double));
+        if (!s_row) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < nrows; ++t) {
+            if (!s_row) continue;
+            const int64_t bh = bh_idx[t], i = row_idx[t];
+            const int64_t last = causal ? Nk - Nq + i : Nk - 1;
+            attention_row_keys(q + (bh * Nq + i) * d, k + bh * Nk * d, v + bh * Nk * d, Nk, d, last,
+                               scale, s_row, o_rows + t * d, lse_rows + t);
+        }
+        free(s_row);
+    }
+    return failed ? -2 : 0;
+}
+
 int oracle_max_threads(void)
 {
     return pick_threads(0);

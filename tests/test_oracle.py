@@ -219,9 +219,56 @@ def pin_online_recurrence(orc):
             np.testing.assert_allclose(l2, lse, rtol=1e-13, atol=1e-12)
 
 
+def pin_rect_is_square_when_nq_is_nk(orc):
+    """Decode attention with as many queries as keys is the square case."""
+    q, k, v = make_random_qkv(2, 2, 29, 16, 31)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.3)
+        o2, l2 = orc.attention_rect(q, k, v, causal, 0.3)
+        np.testing.assert_array_equal(o2, o)
+        np.testing.assert_array_equal(l2, lse)
+
+
+def pin_rect_bottom_right(orc):
+    """Causal decode: the Nq queries are the last Nq positions of the sequence,
+    so their rows equal the last Nq rows of square causal attention."""
+    q, k, v = make_random_qkv(1, 3, 40, 16, 32)
+    for nq in (1, 3, 7):
+        o, lse = orc.attention(q, k, v, True, 0.3)
+        o2, l2 = orc.attention_rect(q[:, :, -nq:].contiguous(), k, v, True, 0.3)
+        np.testing.assert_array_equal(o2, o[:, :, -nq:])
+        np.testing.assert_array_equal(l2, lse[:, :, -nq:])
+
+
+def pin_rect_single_query_library(orc):
+    """One query against the whole cache: scipy's softmax and logsumexp."""
+    q, k, v = make_random_qkv(1, 2, 50, 16, 33, q_mult=2.0)
+    q1 = q[:, :, 5:6].contiguous()
+    o, lse = orc.attention_rect(q1, k, v, False, 0.4)
+    S = 0.4 * np.einsum("bhqc,bhkc->bhqk", f64(q1), f64(k))
+    np.testing.assert_allclose(o, np.einsum("bhqk,bhkc->bhqc", scipy.special.softmax(S, axis=-1), f64(v)),
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, scipy.special.logsumexp(S, axis=-1), rtol=1e-13, atol=1e-12)
+
+
+def pin_rect_rows_entry(orc):
+    """Selected decode rows equal the same rows of the full computation."""
+    q, k, v = make_random_qkv(2, 2, 33, 16, 34)
+    q4 = q[:, :, :4].contiguous()
+    bh = np.array([0, 3, 1, 2, 3], np.int64)
+    row = np.array([0, 3, 2, 1, 0], np.int64)
+    for causal in (False, True):
+        o, lse = orc.attention_rect(q4, k, v, causal, 0.3)
+        orow, lrow = orc.attention_rect_rows(q4, k, v, causal, 0.3, bh, row)
+        np.testing.assert_array_equal(orow, o.reshape(4, 4, 16)[bh, row])
+        np.testing.assert_array_equal(lrow, lse.reshape(4, 4)[bh, row])
+
+
 PINS = [pin_library_softmax, pin_single_key, pin_equal_scores, pin_two_keys,
         pin_probability_rows, pin_constant_values, pin_score_shift, pin_key_permutation,
-        pin_causal_prefix, pin_huge_scores, pin_rows_entry, pin_online_recurrence]
+        pin_causal_prefix, pin_huge_scores, pin_rows_entry, pin_online_recurrence,
+        pin_rect_is_square_when_nq_is_nk, pin_rect_bottom_right, pin_rect_single_query_library,
+        pin_rect_rows_entry]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -253,6 +300,12 @@ MUTANTS = [
     ("recurrence: denominator not rescaled", "l = l * corr + psum;", "l = l + psum;"),
     ("recurrence: causal tile skip off by one", "if (causal && j0 > i) break;",
      "if (causal && j0 >= i) break;"),
+    ("decode: the query's own key masked", "if (j > last_key) {", "if (j >= last_key) {"),
+    ("decode: causal window aligned top-left",
+     "const int64_t bh = r / Nq, i = r % Nq;\n            const int64_t last = causal ? Nk - Nq + i : Nk - 1;",
+     "const int64_t bh = r / Nq, i = r % Nq;\n            const int64_t last = causal ? i : Nk - 1;"),
+    ("decode: every row uses the head's first query", "attention_row_keys(q + r * d, k + bh * Nk * d",
+     "attention_row_keys(q + bh * Nq * d, k + bh * Nk * d"),
 ]
 
 
