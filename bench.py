@@ -43,6 +43,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak, causal & non-causal"
+DECODE_METRIC = "attention decode (split-KV): KV-cache bytes read per second"
 
 KERNEL_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload
@@ -228,12 +229,178 @@ def cpu_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
                       f"{total_t:.1f} s; FLOPs = 4*d*visible keys per row"}
 
 
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one decode step: K and V read once, q read, O and
+    the logsumexp written."""
+    return 2 * w.B * w.H * w.Nk * w.d * 2 + 2 * w.B * w.H * w.Nq * w.d * 2 + w.B * w.H * w.Nq * 4
+
+
+def decode_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
+    """The fp64 oracle on a bounded random sample of query rows of the same
+    decode workload; bytes of K and V per row processed per second."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    row_bytes = 2 * w.Nk * w.d * 2
+
+    def run(n):
+        bh = rng.integers(0, w.B * w.H, size=n, dtype=np.int64)
+        row = rng.integers(0, w.Nq, size=n, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_rect_rows(q, k, v, w.causal, w.scale, bh, row)
+        return time.perf_counter() - t0
+
+    n = 4
+    dt = run(n)
+    while dt < min(0.5, budget_s / 4) and n < (1 << 16):  # calibrate
+        n *= 2
+        dt = run(n)
+    if dt < budget_s / 2:  # then one sample sized to the budget
+        n = max(n, int(n * budget_s / max(dt, 1e-9)))
+        dt = run(n)
+    return n, dt, n * row_bytes / dt / 1e9
+
+
+def run_decode(args, w, rank, world, local):
+    """One step = one fa_decode call over the whole (B, H, Nk) cache."""
+    import torch
+    import torch.distributed as distm
+
+    import io_aware_attention_gb300 as fa
+    from io_aware_attention_gb300.workloads import make_decode_qkv
+
+    nbytes = decode_bytes(w)
+    config = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+              "scale": "1/sqrt(d)", "inputs": "Q,K,V iid N(0,1) bf16, seeded", "per_gpu_problem": True,
+              "parallelism": f"replicas x{args.gpus}",
+              "l2": f"K,V {2 * w.B * w.H * w.Nk * w.d * 2 / 1e6:.0f} MB > 129 MB L2 (no flush)"}
+    q_h, k_h, v_h = make_decode_qkv(w)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        steps, warm = args.steps, max(args.warmup, 3)
+        for _ in range(warm):
+            decode_oracle_rate(w, q_h, k_h, v_h, 0.2)
+        tot_b, tot_t, n_rows = 0.0, 0.0, 0
+        for _ in range(steps):
+            n, dt, _ = decode_oracle_rate(w, q_h, k_h, v_h, 0.5)
+            tot_b += n * 2 * w.Nk * w.d * 2
+            tot_t += dt
+            n_rows = n
+        value = tot_b / tot_t / 1e9
+        line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": steps, "warmup": warm, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                                 "sample": f"{n_rows} random (b,h,row) query rows per step, fp64 two-pass oracle; "
+                                           "bytes = K and V of the rows' heads"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        distm.init_process_group("nccl", device_id=dev)
+        pg = True
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    ws_bytes = fa.decode_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d, w.causal)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2 if ws_bytes else 1
+
+    for _ in range(max(args.warmup, 3)):
+        fa.decode_into(q, k, v, o, lse, ws, w.causal, w.scale)
+    torch.cuda.synchronize()
+    if fa.check_device_status() != 0:
+        raise RuntimeError("decode reported an error during warm-up")
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg:
+        distm.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fa.decode_into(q, k, v, o, lse, ws, w.causal, w.scale)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        distm.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    ms_per_step = ms / args.steps
+    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+        op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        n_e2e = max(3, min(args.steps, 5))
+
+        def e2e_step():
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+            fa.decode_into(q, k, v, o, lse, ws, w.causal, w.scale)
+            op.copy_(o, non_blocking=True)
+            lp.copy_(lse, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": nbytes * world / (ems / n_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems / n_e2e,
+               "steps": n_e2e, "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
+               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()}
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"hbm_gbs (copy), {peak_src}",
+            "kernel": f"fa::dec::fa_decode_partial_kernel<{w.d},*> + combine", "traffic": None,
+            "alg_bytes_per_launch": nbytes}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        n, dt, rate = decode_oracle_rate(w, q_h, k_h, v_h, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"{n} random (b,h,row) query rows, fp64, {dt:.1f} s; bytes = K and V of each row's head"}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg:
+        distm.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     from io_aware_attention_gb300 import iomodel
-    from io_aware_attention_gb300.workloads import HEADLINE, WORKLOADS, Workload
+    from io_aware_attention_gb300.workloads import DECODE_WORKLOADS, HEADLINE, WORKLOADS, Workload
 
+    if args.workload in DECODE_WORKLOADS:
+        return run_decode(args, DECODE_WORKLOADS[args.workload], rank, world, local)
     wname = args.workload or HEADLINE
     w = WORKLOADS[wname]
     if args.batch:

@@ -21,6 +21,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -72,6 +73,52 @@ typedef enum fa_status {
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                  int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * fa_decode_workspace_bytes — workspace that fa_decode needs for these sizes
+ * on the current device (0 when the key range is not split).  Arguments as
+ * for fa_decode.  FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED as fa_decode
+ * reports them; FA_ERR_CUDA if the device cannot be queried.
+ */
+fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
+                                    int causal, size_t *bytes);
+
+/*
+ * fa_decode — attention of a few query rows against a long key/value cache
+ * ("Fusion and IO-aware kernels", section "Where it breaks": decode reads the
+ * whole KV cache per query token; split-K variants (FlashDecoding)
+ * parallelise across the sequence).  The key range is cut into chunks, each
+ * chunk's online softmax ("Kernels — fusion and FlashAttention" §3) gives a
+ * partial output and logsumexp, and the chunks are merged exactly by their
+ * logsumexps.
+ *
+ * For query row i of (b, h):
+ *     O_i = sum_j softmax_j(scale * q_i . k_j) * v_j,  L_i = ln sum_j exp(scale * q_i . k_j)
+ * over keys j = 0 .. Nk-1, or, with causal = 1, j = 0 .. Nk - Nq + i (query i
+ * stands at position Nk - Nq + i: the newest Nq keys belong to the queries).
+ *
+ * Arguments
+ *   q        device pointer, bf16, contiguous (B, H, Nq, d); 1 <= Nq <= 8.
+ *   k, v     device pointers, bf16, contiguous (B, H, Nk, d): the cache.
+ *   o        device pointer, bf16, contiguous (B, H, Nq, d); fully written.
+ *   lse      device pointer, fp32, contiguous (B, H, Nq); fully written.
+ *   B, H     batch and heads, B*H <= 65535.  d: 64 or 128.  causal: 0 or 1
+ *            (1 requires Nq <= Nk).  scale: finite, > 0.
+ *   workspace, workspace_bytes
+ *            device scratch of at least fa_decode_workspace_bytes(...) bytes,
+ *            16-byte aligned (may be NULL when that size is 0).  It holds the
+ *            chunks' partial results between the two kernels of one call and
+ *            must not be shared by calls that may run at the same time.
+ *   stream   CUDA stream the work is enqueued on.
+ *
+ * Ownership: the caller allocates every buffer, including the workspace; the
+ * library allocates nothing.  Asynchrony as for fa_fwd.  Errors: as fa_fwd,
+ * plus FA_ERR_INVALID_ARG for a missing or short workspace and
+ * FA_ERR_UNSUPPORTED for Nq > 8.
+ */
+fa_status fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
+                    int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                    void *workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * fa_check_device_status — synchronises `stream`, reads and clears the

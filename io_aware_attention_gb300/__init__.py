@@ -18,13 +18,13 @@ import os
 
 from . import _build
 
-__all__ = ["fwd", "fwd_into", "check_device_status", "set_wait_limit_ns", "debug_skip_k_tile", "FaError",
-           "library", "library_path", "version", "STATUS"]
+__all__ = ["fwd", "fwd_into", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
+           "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT"}
-EXPORTS = ["fa_fwd", "fa_check_device_status", "fa_set_wait_limit_ns", "fa_debug_skip_k_tile",
-           "fa_status_string", "fa_version"]
+EXPORTS = ["fa_fwd", "fa_decode", "fa_decode_workspace_bytes", "fa_check_device_status",
+           "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
 
 
 class FaError(RuntimeError):
@@ -54,6 +54,12 @@ def library():
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp]
     lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp,
+                              ctypes.c_size_t, vp]
+    lib.fa_decode.restype = ctypes.c_int
+    lib.fa_decode_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_decode_workspace_bytes.restype = ctypes.c_int
     lib.fa_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_check_device_status.restype = ctypes.c_int
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
@@ -123,6 +129,63 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
         return fwd_into(q, k, v, o, lse, causal, scale, stream)
+
+
+def _check_decode(q, k, v):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 (B, H, N, d) tensor")
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError(f"q (B, H, Nq, d) and k, v (B, H, Nk, d) expected: {tuple(q.shape)} {tuple(k.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+
+
+def decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool = False) -> int:
+    """Workspace bytes fa_decode needs for these sizes on the current device."""
+    out = ctypes.c_size_t(0)
+    rc = library().fa_decode_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d), int(bool(causal)),
+                                             ctypes.byref(out))
+    if rc != 0:
+        raise FaError(rc, "fa_decode_workspace_bytes")
+    return int(out.value)
+
+
+def decode_into(q, k, v, o, lse, workspace, causal: bool = False, scale: float | None = None, stream=None):
+    """Decode attention into caller-provided o, lse and workspace (a CUDA
+    tensor of at least decode_workspace_bytes bytes, or None when that is 0)."""
+    _check_decode(q, k, v)
+    B, H, Nq, d = (int(s) for s in q.shape)
+    Nk = int(k.shape[2])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = library().fa_decode(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
+                             ctypes.c_void_p(lse.data_ptr()), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
+                             ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_decode")
+    return o, lse
+
+
+def decode(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Attention of q (B, H, Nq, d), Nq <= 8, against the cache k, v
+    (B, H, Nk, d); query i stands at key position Nk - Nq + i.  Returns
+    ``(o (B, H, Nq, d) bf16, lse (B, H, Nq) fp32)``."""
+    import torch
+
+    _check_decode(q, k, v)
+    B, H, Nq, d = (int(s) for s in q.shape)
+    with torch.cuda.device(q.device):
+        nbytes = decode_workspace_bytes(B, H, Nq, int(k.shape[2]), d, causal)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=q.device) if nbytes else None
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        return decode_into(q, k, v, o, lse, ws, causal, scale, stream)
 
 
 def check_device_status(stream=None) -> int:

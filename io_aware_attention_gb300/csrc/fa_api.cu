@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -110,9 +111,146 @@ bool device_is_sm103(int* dev_out)
     return major == 10 && minor == 3;
 }
 
+// ---------------------------------------------------------------- decode
+
+// Query slots of the kernel instance serving nq query rows.
+int decode_slots(int64_t nq) { return nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8; }
+
+struct DecodePlan {
+    int slots, splits, chunk;
+    size_t ws_bytes;  // 0 when splits == 1 (the partial kernel writes the output)
+};
+
+// Splits of the key range: about 8 CTAs per SM over all heads (many short
+// waves, a small tail), each CTA streaming at least 4 rounds of keys.
+DecodePlan decode_plan(int64_t BH, int64_t nq, int64_t nk, int64_t d, int sms)
+{
+    DecodePlan pl;
+    pl.slots = decode_slots(nq);
+    const int round = fa::dec::WARPS * fa::dec::loads_in_flight(pl.slots) * (32 / (int)(d / 8));
+    const int64_t max_splits = std::max<int64_t>(1, (nk + 4 * round - 1) / (4 * round));
+    const int64_t want = std::max<int64_t>(1, (8 * (int64_t)sms + BH - 1) / BH);
+    int64_t splits = std::min<int64_t>(want, max_splits);
+    int64_t chunk = (nk + splits - 1) / splits;
+    chunk = (chunk + round - 1) / round * round;
+    splits = (nk + chunk - 1) / chunk;
+    pl.splits = (int)splits;
+    pl.chunk = (int)chunk;
+    pl.ws_bytes = splits > 1 ? (size_t)(BH * nq * splits) * (size_t)(d + 1) * sizeof(float) : 0;
+    return pl;
+}
+
+fa_status decode_check(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal)
+{
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (Nq > fa::dec::MAX_NQ) return FA_ERR_UNSUPPORTED;
+    const int64_t LIM = (int64_t)1 << 62;
+    if (B > LIM / H || B * H > LIM / Nk || B * H * Nk > LIM / d) return FA_ERR_INVALID_ARG;
+    if (B * H > 65535 || Nk > INT32_MAX / 2) return FA_ERR_INVALID_ARG;  // grid.y, key indices
+    return FA_OK;
+}
+
+template <int D, int QM>
+fa_status launch_decode(const fa::dec::Params& p, int64_t BH, cudaStream_t st)
+{
+    fa::dec::fa_decode_partial_kernel<D, QM>
+        <<<dim3((unsigned)p.splits, (unsigned)BH), fa::dec::THREADS, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (p.splits > 1) {
+        fa::dec::fa_decode_combine_kernel<D><<<(unsigned)(BH * p.nq), D, 0, st>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+template <int D>
+fa_status launch_decode_d(const fa::dec::Params& p, int slots, int64_t BH, cudaStream_t st)
+{
+    switch (slots) {
+    case 1: return launch_decode<D, 1>(p, BH, st);
+    case 2: return launch_decode<D, 2>(p, BH, st);
+    case 4: return launch_decode<D, 4>(p, BH, st);
+    default: return launch_decode<D, 8>(p, BH, st);
+    }
+}
+
+// Decode with an explicit workspace (ws, ws_bytes >= the plan's).
+fa_status decode_run(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, void* ws,
+                     size_t ws_bytes, fa_stream_t stream)
+{
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    fa_status st_chk = decode_check(B, H, Nq, Nk, d, causal);
+    if (st_chk != FA_OK) return st_chk;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                          reinterpret_cast<uintptr_t>(ws);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const size_t qb = (size_t)(BH * Nq * d * 2), kb = (size_t)(BH * Nk * d * 2), lb = (size_t)(BH * Nq * 4);
+    if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) || overlaps(o, qb, lse, lb) ||
+        overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb))
+        return FA_ERR_INVALID_ARG;
+
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
+    const DecodePlan pl = decode_plan(BH, Nq, Nk, d, sms);
+    if (pl.ws_bytes > 0) {
+        if (!ws || ws_bytes < pl.ws_bytes) return FA_ERR_INVALID_ARG;
+        if (overlaps(ws, pl.ws_bytes, o, qb) || overlaps(ws, pl.ws_bytes, lse, lb) || overlaps(ws, pl.ws_bytes, q, qb) ||
+            overlaps(ws, pl.ws_bytes, k, kb) || overlaps(ws, pl.ws_bytes, v, kb))
+            return FA_ERR_INVALID_ARG;
+    }
+
+    fa::dec::Params p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.v = static_cast<const __nv_bfloat16*>(v);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.ws_o = static_cast<float*>(ws);
+    p.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(ws) + (size_t)(BH * Nq * pl.splits) * (size_t)d : nullptr;
+    p.nq = (int)Nq;
+    p.nk = (int)Nk;
+    p.splits = pl.splits;
+    p.chunk = pl.chunk;
+    p.causal = causal;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return d == 128 ? launch_decode_d<128>(p, pl.slots, BH, st) : launch_decode_d<64>(p, pl.slots, BH, st);
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                                    size_t* bytes)
+{
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    fa_status st = decode_check(B, H, Nq, Nk, d, causal);
+    if (st != FA_OK) return st;
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
+    *bytes = decode_plan(B * H, Nq, Nk, d, sms).ws_bytes;
+    return FA_OK;
+}
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+                    int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, void* workspace,
+                    size_t workspace_bytes, fa_stream_t stream)
+{
+    return decode_run(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, workspace, workspace_bytes, stream);
+}
+
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                  int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream)

@@ -104,3 +104,64 @@ def sample_rows(w: Workload, n: int | None = None):
     if n >= 2:
         bh[1], row[1] = w.B * w.H - 1, w.N - 1
     return bh, row
+
+
+# ----------------------------------------------------------------- decode
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """Nq query rows per (batch, head) against a cache of Nk keys.
+
+    Drawn like :class:`Workload`: ``torch.Generator('cpu').manual_seed(seed)``,
+    ``torch.randn`` in fp32 in the order Q (B, H, Nq, d), K, V (B, H, Nk, d),
+    then rounded to bf16.
+    """
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+    sample_rows: int = 0  # rows compared with the oracle; 0 = all
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / np.sqrt(self.d)))
+
+
+DECODE_WORKLOADS = {
+    w.name: w
+    for w in (
+        # One new token per sequence against a 32k-token cache of the pages'
+        # B = 8, h = 32, d_head = 128 model: 4.3 GB of K and V per step.
+        DecodeWorkload("decode_b8_h32_nk32768_d128", 8, 32, 1, 32768, 128, False, 2001, sample_rows=64),
+        DecodeWorkload("decode_b2_h4_nq4_nk1000_d64_causal", 2, 4, 4, 1000, 64, True, 2002),
+    )
+}
+
+
+def make_decode_qkv(w: DecodeWorkload, device="cpu"):
+    """Seeded bf16 q (B, H, Nq, d) and cache k, v (B, H, Nk, d)."""
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    q = torch.randn((w.B, w.H, w.Nq, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.H, w.Nk, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.H, w.Nk, w.d), generator=g, dtype=torch.float32)
+    out = [t.to(torch.bfloat16) for t in (q, k, v)]
+    del q, k, v
+    if device != "cpu":
+        out = [t.to(device) for t in out]
+    return tuple(out)
+
+
+def sample_decode_rows(w: DecodeWorkload, n: int | None = None):
+    """Seeded (bh, query row) pairs, including the first and the last."""
+    n = w.sample_rows if n is None else n
+    rng = np.random.default_rng(w.seed + 1)
+    bh = rng.integers(0, w.B * w.H, size=n, dtype=np.int64)
+    row = rng.integers(0, w.Nq, size=n, dtype=np.int64)
+    if n >= 1:
+        bh[0], row[0] = 0, 0
+    if n >= 2:
+        bh[1], row[1] = w.B * w.H - 1, w.Nq - 1
+    return bh, row

@@ -79,3 +79,29 @@ def test_debug_hook_setter(lib):
     assert lib.fa_debug_skip_k_tile(-2) == 1
     assert lib.fa_debug_skip_k_tile(3) == 0
     assert lib.fa_debug_skip_k_tile(-1) == 0
+
+
+def call_decode(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, Nq=1, Nk=64, d=128, causal=0,
+                scale=0.125, ws=6 * P, ws_bytes=1 << 20):
+    vp = ctypes.c_void_p
+    return lib.fa_decode(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, Nq, Nk, d, causal, scale, vp(ws), ws_bytes,
+                         None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(B=0), 1), (dict(Nq=0), 1), (dict(Nk=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
+    (dict(causal=1, Nq=4, Nk=3), 1),   # the causal window needs Nq <= Nk
+    (dict(d=96), 2), (dict(Nq=9), 2),  # head size, more than 8 query rows
+    (dict(q=P + 8), 2), (dict(lse=5 * P + 2), 2), (dict(ws=6 * P + 4), 2),
+    (dict(o=3 * P + 16), 1),           # o overlaps v
+    (dict(B=70000), 1),                # B*H over the grid's 65535
+])
+def test_bad_decode_arguments_are_rejected(lib, kw, status):
+    assert call_decode(lib, **kw) == status
+
+
+def test_decode_workspace_query_checks_arguments(lib):
+    out = ctypes.c_size_t(0)
+    assert lib.fa_decode_workspace_bytes(1, 1, 9, 64, 128, 0, ctypes.byref(out)) == 2
+    assert lib.fa_decode_workspace_bytes(1, 1, 1, 64, 128, 0, None) == 1
