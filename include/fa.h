@@ -40,7 +40,9 @@ typedef enum fa_status {
     FA_ERR_UNSUPPORTED = 2,  /* head size not 64/128, pointer not 16-byte aligned
                                 (lse: 4-byte), device not sm_103 */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
-    FA_ERR_TIMEOUT = 4       /* a kernel gave up a pipeline wait (device status) */
+    FA_ERR_TIMEOUT = 4,      /* a kernel gave up a pipeline wait (device status) */
+    FA_ERR_TOO_LARGE = 5     /* fa_decode_static: the sizes need more scratch than
+                                FA_DECODE_STATIC_SCRATCH_BYTES */
 } fa_status;
 
 /*
@@ -119,6 +121,36 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
 fa_status fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                     int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
                     void *workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * fa_decode_static — fa_decode without a caller workspace and without any
+ * allocation.  The pages have no counterpart to this entry point: it exists
+ * for callers that cannot hand over device memory at the point of the call,
+ * for instance a runtime whose own pool already owns all device memory, or
+ * code that must not call cudaMalloc/cudaFree because those calls can
+ * synchronise the device.  The chunks' partial results go to a scratch array
+ * compiled into the library (a static device array of
+ * FA_DECODE_STATIC_SCRATCH_BYTES, 8 MiB), so nothing is allocated by this
+ * call or by the library.
+ *
+ *   - Arguments, results and errors are those of fa_decode, minus the
+ *     workspace; sizes whose scratch need (fa_decode_workspace_bytes) exceeds
+ *     FA_DECODE_STATIC_SCRATCH_BYTES are rejected with FA_ERR_TOO_LARGE and
+ *     nothing is enqueued.
+ *   - The first call on a device looks up the device address of the scratch
+ *     array (cudaGetSymbolAddress, with that device current; a failure is
+ *     returned as FA_ERR_CUDA), which may load the library's device code.  Make
+ *     that first call on each device before any stream capture begins.
+ *   - There is one scratch array per device.  Calls that may run at the same
+ *     time on one device (other streams, other host threads) overwrite each
+ *     other's partial results: order them, e.g. on one stream.
+ *   - Nothing in the scratch needs to start at zero: each call writes every
+ *     partial result before reading it.
+ */
+#define FA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+fa_status fa_decode_static(const void *q, const void *k, const void *v, void *o, float *lse,
+                           int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
+                           float scale, fa_stream_t stream);
 
 /*
  * fa_check_device_status — synchronises `stream`, reads and clears the

@@ -22,8 +22,8 @@ __all__ = ["fwd", "fwd_into", "decode", "decode_into", "decode_workspace_bytes",
            "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
-          4: "FA_ERR_TIMEOUT"}
-EXPORTS = ["fa_fwd", "fa_decode", "fa_decode_workspace_bytes", "fa_check_device_status",
+          4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
+EXPORTS = ["fa_fwd", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
            "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
 
 
@@ -60,6 +60,9 @@ def library():
     lib.fa_decode_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int,
                                               ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_decode_workspace_bytes.restype = ctypes.c_int
+    lib.fa_decode_static.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                                     vp]
+    lib.fa_decode_static.restype = ctypes.c_int
     lib.fa_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_check_device_status.restype = ctypes.c_int
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]

@@ -226,9 +226,49 @@ fa_status decode_run(const void* q, const void* k, const void* v, void* o, float
     return d == 128 ? launch_decode_d<128>(p, pl.slots, BH, st) : launch_decode_d<64>(p, pl.slots, BH, st);
 }
 
+// Scratch of fa_decode_static: compiled into the library, one per device.
+static __device__ __align__(256) unsigned char g_decode_scratch[FA_DECODE_STATIC_SCRATCH_BYTES];
+
+// Device address of g_decode_scratch on device `dev` (the current device),
+// looked up once per device.
+void* static_scratch(int dev)
+{
+    static std::atomic<void*> cache[MAX_DEVICES];
+    static std::mutex lock;
+    if (dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    void* p = cache[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    std::lock_guard<std::mutex> guard(lock);
+    p = cache[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+        cache[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_decode_static(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                           int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
+                           fa_stream_t stream)
+{
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    fa_status st = decode_check(B, H, Nq, Nk, d, causal);
+    if (st != FA_OK) return st;
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
+    const size_t need = decode_plan(B * H, Nq, Nk, d, sms).ws_bytes;
+    if (need > FA_DECODE_STATIC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
+    void* scratch = static_scratch(dev);
+    if (!scratch) return FA_ERR_CUDA;
+    return decode_run(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, scratch, FA_DECODE_STATIC_SCRATCH_BYTES,
+                      stream);
+}
 
 fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal,
                                     size_t* bytes)
@@ -353,6 +393,7 @@ const char* fa_status_string(fa_status s)
     case FA_ERR_UNSUPPORTED: return "unsupported (head size, alignment or device)";
     case FA_ERR_CUDA: return "CUDA error";
     case FA_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case FA_ERR_TOO_LARGE: return "the sizes need more scratch than the library's static array holds";
     }
     return "unknown status";
 }

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(5):
+    for code in range(6):
         s = lib.fa_status_string(code)
         assert s and s != b"unknown status"
     assert lib.fa_status_string(99) == b"unknown status"
@@ -99,6 +99,15 @@ def call_decode(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, Nq=1, 
 ])
 def test_bad_decode_arguments_are_rejected(lib, kw, status):
     assert call_decode(lib, **kw) == status
+
+
+def test_static_decode_checks_arguments_first(lib):
+    vp = ctypes.c_void_p
+    # bad arguments are refused before any device call
+    assert lib.fa_decode_static(vp(0), vp(2 * P), vp(3 * P), vp(4 * P), vp(5 * P), 1, 1, 1, 64, 128, 0, 0.1,
+                                None) == 1
+    assert lib.fa_decode_static(vp(P), vp(2 * P), vp(3 * P), vp(4 * P), vp(5 * P), 1, 1, 9, 64, 128, 0, 0.1,
+                                None) == 2
 
 
 def test_decode_workspace_query_checks_arguments(lib):
