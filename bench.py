@@ -400,7 +400,12 @@ def main(argv=None):
     from io_aware_attention_gb300.workloads import DECODE_WORKLOADS, HEADLINE, WORKLOADS, Workload
 
     if args.workload in DECODE_WORKLOADS:
-        return run_decode(args, DECODE_WORKLOADS[args.workload], rank, world, local)
+        wd = DECODE_WORKLOADS[args.workload]
+        if args.batch:
+            from io_aware_attention_gb300.workloads import DecodeWorkload
+            wd = DecodeWorkload(wd.name + f"_b{args.batch}", args.batch, wd.H, wd.Nq, wd.Nk, wd.d, wd.causal, wd.seed,
+                                wd.sample_rows)
+        return run_decode(args, wd, rank, world, local)
     wname = args.workload or HEADLINE
     w = WORKLOADS[wname]
     if args.batch:
