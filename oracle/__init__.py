@@ -17,6 +17,10 @@ and "Writing and Benchmarking Custom Kernels" §10.3.1):
 ``attention_online`` runs the tile-by-tile online-softmax recurrence of
 "Kernels — fusion and FlashAttention" §3 instead, in fp64.
 
+``attention_bwd`` gives the gradients dQ, dK, dV (and the per-row scalar
+D_i) for a given dO, by the softmax/matrix-product chain rule that
+"Writing and Benchmarking Custom Kernels" §10.3.2 describes.
+
 Inputs are torch bf16 CPU tensors (or numpy uint16 arrays of bf16 bits) of
 shape (B, H, N, d), contiguous.  Outputs are numpy float64.
 """
@@ -87,8 +91,11 @@ class Oracle:
         rect = [u16p, u16p, u16p, i64, i64, i64, i64, i64, c_int, c_dbl]
         lib.oracle_attn_rect_f64.argtypes = rect + [f64p, f64p, c_int]
         lib.oracle_attn_rect_rows_f64.argtypes = rect + [i64p, i64p, i64, f64p, f64p, c_int]
+        lib.oracle_attn_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, c_int,
+                                            c_dbl, f64p, f64p, f64p, f64p, c_int]
         for fn in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_online_f64,
-                   lib.oracle_max_threads, lib.oracle_attn_rect_f64, lib.oracle_attn_rect_rows_f64):
+                   lib.oracle_max_threads, lib.oracle_attn_rect_f64, lib.oracle_attn_rect_rows_f64,
+                   lib.oracle_attn_bwd_f64):
             fn.restype = c_int
         self.lib = lib
 
@@ -204,6 +211,30 @@ class Oracle:
             raise RuntimeError(f"oracle_attn_rect_rows_f64 failed ({rc})")
         return o, lse
 
+    def attention_bwd(self, q, k, v, do, causal: bool, scale: float, threads: int = 0):
+        """Gradients of square attention for the output gradient ``do``.
+
+        q, k, v, do: bf16 (B, H, N, d).  Returns ``(dq, dk, dv, D)``, the
+        first three (B, H, N, d) and D (B, H, N), all float64.
+        """
+        qb, kb, vb, db = _bits(q), _bits(k), _bits(v), _bits(do)
+        B, H, N, d = _shape4(qb, kb, vb)
+        if db.shape != qb.shape:
+            raise ValueError(f"do must have the shape of q: {db.shape} vs {qb.shape}")
+        dq = np.empty((B, H, N, d), np.float64)
+        dk = np.empty((B, H, N, d), np.float64)
+        dv = np.empty((B, H, N, d), np.float64)
+        dsum = np.empty((B, H, N), np.float64)
+        rc = self.lib.oracle_attn_bwd_f64(_ptr(qb, ctypes.c_uint16), _ptr(kb, ctypes.c_uint16),
+                                          _ptr(vb, ctypes.c_uint16), _ptr(db, ctypes.c_uint16),
+                                          B, H, N, d, int(bool(causal)), float(scale),
+                                          _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double),
+                                          _ptr(dv, ctypes.c_double), _ptr(dsum, ctypes.c_double),
+                                          int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attn_bwd_f64 failed ({rc})")
+        return dq, dk, dv, dsum
+
 
 def _shape_rect(q, k, v):
     if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
@@ -255,3 +286,7 @@ def attention_rect(q, k, v, causal, scale, threads=0):
 
 def attention_rect_rows(q, k, v, causal, scale, bh_idx, row_idx, threads=0):
     return _oracle().attention_rect_rows(q, k, v, causal, scale, bh_idx, row_idx, threads)
+
+
+def attention_bwd(q, k, v, do, causal, scale, threads=0):
+    return _oracle().attention_bwd(q, k, v, do, causal, scale, threads)

@@ -348,3 +348,119 @@ int oracle_max_threads(void)
 {
     return pick_threads(0);
 }
+
+/* ------------------------------------------------------------------------
+ * Backward pass: the gradients of the square attention above with respect
+ * to q, k and v, given the gradient dO of a loss with respect to O.
+ *
+ * Sources: "Writing and Benchmarking Custom Kernels" (arunshar.com, ch. 10),
+ * §10.3.2 "Backward-Pass Recomputation in FlashAttention": the softmax
+ * backward of row i reduces to one scalar per query, D_i, the score
+ * gradient is the probability times (dP minus that scalar), and
+ * dL/dP_ij = dO_i . V_j.  The page's displayed formulas did not survive
+ * extraction, so this is the textbook softmax/matrix-product chain rule,
+ * which the surviving prose describes:
+ *
+ *     P_ij  = the two-pass softmax of the masked, scaled scores (as above)
+ *     dV_j  = sum_i P_ij dO_i
+ *     dP_ij = dO_i . V_j
+ *     D_i   = sum_j P_ij dP_ij          (equal to dO_i . O_i, the page's form)
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dQ_i  = scale * sum_j dS_ij K_j
+ *     dK_j  = scale * sum_i dS_ij Q_i
+ *
+ * One head at a time: P and dS of the head are materialised (2 N^2
+ * doubles), query rows are spread over threads for P, dS, D and dQ, then key
+ * rows for dV and dK.  Inputs are bf16 bits (B, H, N, d) like the forward;
+ * dq, dk, dv: B*H*N*d doubles; dsum (nullable): B*H*N doubles, the D_i.
+ * Returns 0, -1 on bad arguments, -2 when the head's matrices cannot be
+ * allocated.
+ * ------------------------------------------------------------------------ */
+int oracle_attn_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *dout, int64_t B, int64_t H, int64_t N, int64_t d,
+                        int causal, double scale, double *dq, double *dk, double *dv,
+                        double *dsum, int nthreads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || bad_shape(B, H, N, d)) return -1;
+    const int64_t nd = N * d;
+    double *P = (double *)malloc((size_t)(N * N) * sizeof(double));
+    double *dS = (double *)malloc((size_t)(N * N) * sizeof(double));
+    double *Qw = (double *)malloc((size_t)nd * sizeof(double));
+    double *Kw = (double *)malloc((size_t)nd * sizeof(double));
+    double *Vw = (double *)malloc((size_t)nd * sizeof(double));
+    double *dOw = (double *)malloc((size_t)nd * sizeof(double));
+    int failed = !P || !dS || !Qw || !Kw || !Vw || !dOw;
+    for (int64_t bh = 0; bh < B * H && !failed; ++bh) {
+        const int64_t base = bh * nd;
+        for (int64_t t = 0; t < nd; ++t) {
+            Qw[t] = bf16_bits_to_f64(q[base + t]);
+            Kw[t] = bf16_bits_to_f64(k[base + t]);
+            Vw[t] = bf16_bits_to_f64(v[base + t]);
+            dOw[t] = bf16_bits_to_f64(dout[base + t]);
+        }
+#pragma omp parallel num_threads(pick_threads(nthreads))
+        {
+            double *dP = (double *)malloc((size_t)N * sizeof(double));
+            if (!dP) {
+#pragma omp atomic write
+                failed = 1;
+            }
+            /* query rows: P, dP, D, dS and dQ */
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t i = 0; i < N; ++i) {
+                if (!dP) continue;
+                double *Pi = P + i * N, *dSi = dS + i * N;
+                const int64_t visible = causal ? i + 1 : N; /* keys 0 .. visible-1 */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < visible; ++j) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c) dot += Qw[i * d + c] * Kw[j * d + c];
+                    Pi[j] = scale * dot;
+                    if (Pi[j] > m) m = Pi[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j < visible; ++j) {
+                    Pi[j] = exp(Pi[j] - m);
+                    l += Pi[j];
+                }
+                for (int64_t j = 0; j < visible; ++j) Pi[j] /= l;
+                for (int64_t j = visible; j < N; ++j) Pi[j] = 0.0;
+                double Di = 0.0;
+                for (int64_t j = 0; j < visible; ++j) {
+                    double g = 0.0;
+                    for (int64_t c = 0; c < d; ++c) g += dOw[i * d + c] * Vw[j * d + c];
+                    dP[j] = g;
+                    Di += Pi[j] * g;
+                }
+                for (int64_t j = 0; j < N; ++j) dSi[j] = j < visible ? Pi[j] * (dP[j] - Di) : 0.0;
+                if (dsum) dsum[bh * N + i] = Di;
+                for (int64_t c = 0; c < d; ++c) {
+                    double acc = 0.0;
+                    for (int64_t j = 0; j < visible; ++j) acc += dSi[j] * Kw[j * d + c];
+                    dq[base + i * d + c] = scale * acc;
+                }
+            }
+            /* key rows: dV and dK (column j of P and of dS) */
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t j = 0; j < N; ++j) {
+                for (int64_t c = 0; c < d; ++c) {
+                    double gv = 0.0, gk = 0.0;
+                    for (int64_t i = 0; i < N; ++i) {
+                        gv += P[i * N + j] * dOw[i * d + c];
+                        gk += dS[i * N + j] * Qw[i * d + c];
+                    }
+                    dv[base + j * d + c] = gv;
+                    dk[base + j * d + c] = scale * gk;
+                }
+            }
+            free(dP);
+        }
+    }
+    free(P);
+    free(dS);
+    free(Qw);
+    free(Kw);
+    free(Vw);
+    free(dOw);
+    return failed ? -2 : 0;
+}

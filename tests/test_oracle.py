@@ -19,6 +19,18 @@ FlashAttention" §2–§3, "Fusion and IO-aware kernels" § FlashAttention, and
     unmasked problem on its prefix, huge scores do not overflow;
   * the tile-by-tile online recurrence reaches the two-pass result for every
     tile size, including 1, sizes that do not divide N, and sizes above N.
+
+The backward (gradients dQ, dK, dV for a given dO; "Writing and Benchmarking
+Custom Kernels" §10.3.2) is pinned by:
+  * torch's fp64 autograd of the plain masked softmax(QK^T)V expression;
+  * central finite differences (Richardson-extrapolated) of the forward
+    oracle's sum(O * dO), on inputs that are multiples of 2^-7 below 2 in
+    magnitude so that every perturbed input is still exactly a bf16 value;
+  * invariants: the softmax gradient rows sum to zero, so the key gradients
+    sum to zero over keys; the value gradients sum to the summed dO; D_i
+    equals dO_i . O_i (the page's form of the row scalar); a single key gives
+    dV = dO and dQ = dK = 0; under the causal mask keys after the last row
+    with a nonzero dO get no gradient; key permutation permutes dK, dV.
 """
 import math
 import os
@@ -264,11 +276,124 @@ def pin_rect_rows_entry(orc):
         np.testing.assert_array_equal(lrow, lse.reshape(4, 4)[bh, row])
 
 
+def _bwd_inputs(B, H, N, d, seed):
+    """bf16 q, k, v whose entries are multiples of 2^-7 in (-1.9, 1.9), so that
+    x +- 2^-7 and x +- 2^-6 are bf16 values too; dO any bf16."""
+    rng = np.random.default_rng(seed)
+    grid = lambda: bf16(np.clip(np.round(rng.standard_normal((B, H, N, d)) * 0.7 * 128) / 128,
+                                -1.875, 1.875))
+    q, k, v = grid(), grid(), grid()
+    do = bf16(rng.standard_normal((B, H, N, d)))
+    return q, k, v, do
+
+
+def pin_bwd_autograd(orc):
+    """torch fp64 autograd of softmax(scale*QK^T + mask) V with output gradient dO."""
+    for (B, H, N, d, causal, seed) in [(1, 1, 1, 8, True, 41), (1, 2, 6, 8, True, 42),
+                                        (2, 1, 11, 16, False, 43), (1, 1, 13, 32, True, 44)]:
+        q, k, v = make_random_qkv(B, H, N, d, seed, q_mult=1.5)
+        do = make_random_qkv(B, H, N, d, seed + 100)[0]
+        scale = 0.31
+        dq, dk, dv, dsum = orc.attention_bwd(q, k, v, do, causal, scale)
+        Q, K, V = (torch.from_numpy(f64(t)).requires_grad_() for t in (q, k, v))
+        S = scale * Q @ K.transpose(-1, -2)
+        if causal:
+            S = S.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+        O = torch.softmax(S, dim=-1) @ V
+        O.backward(torch.from_numpy(f64(do)))
+        for mine, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+            np.testing.assert_allclose(mine, ref.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def pin_bwd_finite_differences(orc):
+    """Every gradient entry against (8(f(x+h)-f(x-h)) - (f(x+2h)-f(x-2h))) / 12h of
+    f = sum(O * dO) through the forward oracle, h = 2^-7 (error O(h^4))."""
+    h = 2.0 ** -7
+    for (N, d, causal, seed) in [(5, 4, True, 45), (4, 3, False, 46)]:
+        q, k, v, do = _bwd_inputs(1, 1, N, d, seed)
+        scale = 0.35
+        dq, dk, dv, _ = orc.attention_bwd(q, k, v, do, causal, scale)
+        dO = f64(do)
+
+        def f(qq, kk, vv):
+            return float((orc.attention(qq, kk, vv, causal, scale)[0] * dO).sum())
+
+        for which, grad in ((0, dq), (1, dk), (2, dv)):
+            for i in range(N):
+                for c in range(d):
+                    vals = []
+                    for step in (h, -h, 2 * h, -2 * h):
+                        ins = [q.clone(), k.clone(), v.clone()]
+                        ins[which][0, 0, i, c] = ins[which][0, 0, i, c].float() + step
+                        assert float(ins[which][0, 0, i, c]) == float(
+                            [q, k, v][which][0, 0, i, c]) + step  # perturbation is exact
+                        vals.append(f(*ins))
+                    fd = (8 * (vals[0] - vals[1]) - (vals[2] - vals[3])) / (12 * h)
+                    assert abs(grad[0, 0, i, c] - fd) <= 1e-7 + 1e-6 * abs(fd), (which, i, c)
+
+
+def pin_bwd_invariants(orc):
+    """Rows of the softmax gradient sum to zero (so sum_j dK_j = 0), sum_j dV_j
+    = sum_i dO_i, and D_i = dO_i . O_i."""
+    q, k, v = make_random_qkv(2, 2, 21, 16, 47, q_mult=2.0)
+    do = make_random_qkv(2, 2, 21, 16, 48)[0]
+    for causal in (False, True):
+        dq, dk, dv, dsum = orc.attention_bwd(q, k, v, do, causal, 0.4)
+        o, _ = orc.attention(q, k, v, causal, 0.4)
+        scale_dk = np.abs(dk).max()
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, rtol=0, atol=1e-13 * 21 * max(1.0, scale_dk))
+        np.testing.assert_allclose(dv.sum(axis=2), f64(do).sum(axis=2), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dsum, (f64(do) * o).sum(-1), rtol=1e-12, atol=1e-12)
+
+
+def pin_bwd_single_key(orc):
+    """N = 1: P = 1, so dV = dO and the score gradient, hence dQ and dK, is zero."""
+    q, k, v = make_random_qkv(2, 2, 1, 32, 49)
+    do = make_random_qkv(2, 2, 1, 32, 50)[0]
+    for causal in (False, True):
+        dq, dk, dv, _ = orc.attention_bwd(q, k, v, do, causal, 0.2)
+        np.testing.assert_array_equal(dv, f64(do))
+        np.testing.assert_array_equal(dq, 0.0)
+        np.testing.assert_array_equal(dk, 0.0)
+
+
+def pin_bwd_causal_tail(orc):
+    """Causal, dO zero from row t on: keys t.. are seen only by those rows, so
+    their dK and dV are zero; rows before t match the problem cut at t."""
+    q, k, v = make_random_qkv(1, 2, 17, 16, 51)
+    do = make_random_qkv(1, 2, 17, 16, 52)[0]
+    t = 9
+    do[:, :, t:] = 0
+    dq, dk, dv, _ = orc.attention_bwd(q, k, v, do, True, 0.3)
+    np.testing.assert_array_equal(dk[:, :, t:], 0.0)
+    np.testing.assert_array_equal(dv[:, :, t:], 0.0)
+    np.testing.assert_array_equal(dq[:, :, t:], 0.0)
+    cut = [x[:, :, :t].contiguous() for x in (q, k, v, do)]
+    dq2, dk2, dv2, _ = orc.attention_bwd(*cut, True, 0.3)
+    for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):
+        np.testing.assert_allclose(a[:, :, :t], b, rtol=1e-13, atol=1e-14)
+
+
+def pin_bwd_key_permutation(orc):
+    """Non-causal: permuting the (key, value) pairs permutes dK and dV the same
+    way and leaves dQ alone."""
+    q, k, v = make_random_qkv(1, 1, 15, 8, 53)
+    do = make_random_qkv(1, 1, 15, 8, 54)[0]
+    perm = torch.from_numpy(np.random.default_rng(55).permutation(15))
+    dq, dk, dv, _ = orc.attention_bwd(q, k, v, do, False, 0.5)
+    dq2, dk2, dv2, _ = orc.attention_bwd(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(),
+                                         do, False, 0.5)
+    np.testing.assert_allclose(dq2, dq, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dk2, dk[:, :, perm.numpy()], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv2, dv[:, :, perm.numpy()], rtol=1e-12, atol=1e-13)
+
+
 PINS = [pin_library_softmax, pin_single_key, pin_equal_scores, pin_two_keys,
         pin_probability_rows, pin_constant_values, pin_score_shift, pin_key_permutation,
         pin_causal_prefix, pin_huge_scores, pin_rows_entry, pin_online_recurrence,
         pin_rect_is_square_when_nq_is_nk, pin_rect_bottom_right, pin_rect_single_query_library,
-        pin_rect_rows_entry]
+        pin_rect_rows_entry, pin_bwd_autograd, pin_bwd_finite_differences, pin_bwd_invariants,
+        pin_bwd_single_key, pin_bwd_causal_tail, pin_bwd_key_permutation]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -306,6 +431,22 @@ MUTANTS = [
      "const int64_t bh = r / Nq, i = r % Nq;\n            const int64_t last = causal ? i : Nk - 1;"),
     ("decode: every row uses the head's first query", "attention_row_keys(q + r * d, k + bh * Nk * d",
      "attention_row_keys(q + bh * Nq * d, k + bh * Nk * d"),
+    ("backward: D dropped", "dSi[j] = j < visible ? Pi[j] * (dP[j] - Di) : 0.0;",
+     "dSi[j] = j < visible ? Pi[j] * dP[j] : 0.0;"),
+    ("backward: score gradient sign", "dSi[j] = j < visible ? Pi[j] * (dP[j] - Di) : 0.0;",
+     "dSi[j] = j < visible ? Pi[j] * (Di - dP[j]) : 0.0;"),
+    ("backward: D without the probabilities", "Di += Pi[j] * g;", "Di += g;"),
+    ("backward: dQ scale dropped", "dq[base + i * d + c] = scale * acc;", "dq[base + i * d + c] = acc;"),
+    ("backward: dQ from the values", "acc += dSi[j] * Kw[j * d + c];", "acc += dSi[j] * Vw[j * d + c];"),
+    ("backward: dK from dS untransposed", "gk += dS[i * N + j] * Qw[i * d + c];",
+     "gk += dS[j * N + i] * Qw[i * d + c];"),
+    ("backward: dK from dO", "gk += dS[i * N + j] * Qw[i * d + c];", "gk += dS[i * N + j] * dOw[i * d + c];"),
+    ("backward: dV from P untransposed", "gv += P[i * N + j] * dOw[i * d + c];",
+     "gv += P[j * N + i] * dOw[i * d + c];"),
+    ("backward: diagonal masked", "const int64_t visible = causal ? i + 1 : N;",
+     "const int64_t visible = causal ? (i > 0 ? i : 1) : N;"),
+    ("backward: dP from the keys", "for (int64_t c = 0; c < d; ++c) g += dOw[i * d + c] * Vw[j * d + c];",
+     "for (int64_t c = 0; c < d; ++c) g += dOw[i * d + c] * Kw[j * d + c];"),
 ]
 
 
