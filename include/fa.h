@@ -153,6 +153,54 @@ fa_status fa_decode_static(const void *q, const void *k, const void *v, void *o,
                            float scale, fa_stream_t stream);
 
 /*
+ * fa_bwd_workspace_bytes — device scratch that fa_bwd needs for these sizes:
+ * B*H*Np*(d + 2)*4 bytes, Np = N rounded up to a multiple of 64 (the per-row
+ * L*log2 e and D, and the fp32 dQ accumulator).  Needs no device.  Errors:
+ * FA_ERR_INVALID_ARG (bytes NULL, sizes < 1 or too large),
+ * FA_ERR_UNSUPPORTED (d other than 128).
+ */
+fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes);
+
+/*
+ * fa_bwd — gradients of fa_fwd's attention with respect to q, k and v for
+ * the output gradient dout ("Writing and Benchmarking Custom Kernels"
+ * §10.3.2, backward-pass recomputation): the probabilities are recomputed
+ * tile by tile from the forward's logsumexp, never stored.  For each (b, h),
+ * with P the attention probabilities of fa_fwd and L its logsumexp:
+ *     D_i   = dO_i . O_i
+ *     dV_j  = sum_i P_ij dO_i
+ *     dS_ij = P_ij (dO_i . V_j - D_i)
+ *     dQ_i  = scale * sum_j dS_ij K_j,   dK_j = scale * sum_i dS_ij Q_i
+ * (sums over the pairs the mask lets through: j <= i when causal).
+ *
+ * Arguments
+ *   q, k, v    device pointers, bf16, contiguous (B, H, N, d): the forward's inputs.
+ *   o, lse     the forward's outputs for those inputs (o bf16 (B, H, N, d),
+ *              lse fp32 (B, H, N), natural log); same causal and scale.
+ *   dout       device pointer, bf16, contiguous (B, H, N, d): dLoss/dO.
+ *   dq, dk, dv device pointers, bf16, contiguous (B, H, N, d); fully written.
+ *   d          128.  causal: 0 or 1.  scale: finite, > 0 (the forward's).
+ *   workspace, workspace_bytes
+ *              device scratch of at least fa_bwd_workspace_bytes(...) bytes,
+ *              16-byte aligned; nothing in it needs to start at zero.  Calls
+ *              that may run at the same time must not share it.
+ *   stream     CUDA stream the three kernels (prepare, main, dQ convert) are
+ *              enqueued on.
+ *
+ * Ownership: the caller owns every buffer; the library allocates nothing.
+ * Bf16 pointers and the workspace 16-byte aligned, lse 4-byte aligned,
+ * else FA_ERR_UNSUPPORTED.  Outputs and workspace may overlap no input and
+ * no other output (FA_ERR_INVALID_ARG).  Asynchrony, FA_ERR_CUDA and
+ * FA_ERR_TIMEOUT reporting as for fa_fwd.  dQ is accumulated in fp32 with
+ * element-wise atomic adds, so its last bits may differ between runs; dK and
+ * dV are deterministic.
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N,
+                 int64_t d, int causal, float scale, void *workspace, size_t workspace_bytes,
+                 fa_stream_t stream);
+
+/*
  * fa_check_device_status — synchronises `stream`, reads and clears the
  * device-side status word of the current device.  Returns FA_ERR_TIMEOUT if a
  * kernel launched since the last check gave up a bounded wait (its outputs are

@@ -9,6 +9,11 @@ is missing or the device is not sm_103, calls raise.
 q, k, v: CUDA bf16 tensors of shape (B, H, N, d), contiguous, d in {64, 128}.
 Returns o (bf16, same shape) and lse (fp32, (B, H, N)), the natural-log
 logsumexp of each row's scaled, masked scores.
+
+    dq, dk, dv = io_aware_attention_gb300.bwd(q, k, v, o, lse, do, causal=True)
+
+gives the gradients for the output gradient ``do`` (d = 128), recomputing the
+probabilities from ``lse``.
 """
 from __future__ import annotations
 
@@ -18,12 +23,12 @@ import os
 
 from . import _build
 
-__all__ = ["fwd", "fwd_into", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
+__all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
            "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
-EXPORTS = ["fa_fwd", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
+EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
            "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
 
 
@@ -54,6 +59,11 @@ def library():
     vp, i64 = ctypes.c_void_p, ctypes.c_int64
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp]
     lib.fa_fwd.restype = ctypes.c_int
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float,
+                           vp, ctypes.c_size_t, vp]
+    lib.fa_bwd.restype = ctypes.c_int
+    lib.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_int
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp,
                               ctypes.c_size_t, vp]
     lib.fa_decode.restype = ctypes.c_int
@@ -132,6 +142,55 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
         o = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
         return fwd_into(q, k, v, o, lse, causal, scale, stream)
+
+
+def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    """Workspace bytes fa_bwd needs for these sizes."""
+    out = ctypes.c_size_t(0)
+    rc = library().fa_bwd_workspace_bytes(int(B), int(H), int(N), int(d), ctypes.byref(out))
+    if rc != 0:
+        raise FaError(rc, "fa_bwd_workspace_bytes")
+    return int(out.value)
+
+
+def bwd_into(q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False, scale: float | None = None,
+             stream=None):
+    """Backward into caller-provided dq, dk, dv (bf16) and workspace (a CUDA
+    tensor of at least bwd_workspace_bytes bytes)."""
+    import torch
+
+    _check(q, k, v)
+    _check(o, do, dq)
+    _check(dk, dv, dq)
+    if not (q.shape == o.shape == do.shape == dq.shape):
+        raise ValueError("o, do, dq, dk, dv must have the shape of q")
+    B, H, N, d = (int(s) for s in q.shape)
+    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be a contiguous CUDA fp32 (B, H, N) tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    vp = ctypes.c_void_p
+    rc = library().fa_bwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()),
+                          vp(lse.data_ptr()), vp(do.data_ptr()), vp(dq.data_ptr()), vp(dk.data_ptr()),
+                          vp(dv.data_ptr()), B, H, N, d, int(bool(causal)), float(scale), vp(workspace.data_ptr()),
+                          ws_bytes, _stream_handle(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, stream=None):
+    """Gradients ``(dq, dk, dv)`` of the attention forward (o, lse from
+    :func:`fwd` with the same causal and scale) for the output gradient do."""
+    import torch
+
+    _check(q, k, v)
+    B, H, N, d = (int(s) for s in q.shape)
+    with torch.cuda.device(q.device):
+        ws = torch.empty(bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+        return bwd_into(q, k, v, o, lse, do, dq, dk, dv, ws, causal, scale, stream)
 
 
 def _check_decode(q, k, v):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_bwd_kernel.cuh"
 #include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
@@ -56,6 +57,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The backward's fp32 dQ accumulator (B*H, Np, d) as a 3-D tensor; box = 32
+// columns x 64 rows x 1 head, no swizzle (the reduce-add source is a plain
+// row-major 64 x 32 block).
+bool make_acc_map(CUtensorMap* map, void* base, int64_t BH, int64_t Np, int64_t d)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Np, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * 4), (cuuint64_t)(Np * d * 4)};
+    cuuint32_t box[3] = {32, (cuuint32_t)fa::bwd::BQ, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb)
@@ -109,6 +126,55 @@ bool device_is_sm103(int* dev_out)
         return false;
     *dev_out = dev;
     return major == 10 && minor == 3;
+}
+
+// -------------------------------------------------------------- backward
+
+template <int D, bool CAUSAL>
+cudaError_t prepare_bwd_kernel(int dev)
+{
+    static std::atomic<int> done[MAX_DEVICES];
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fa::bwd::fa_bwd_kernel<D, CAUSAL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)fa::bwd::Layout<D>::SMEM_BYTES);
+    if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
+    return e;
+}
+
+struct BwdShape {
+    int64_t BH, Np, num_kb;
+    size_t ws_bytes;
+};
+
+fa_status bwd_check(int64_t B, int64_t H, int64_t N, int64_t d, BwdShape* sh)
+{
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t LIM = (int64_t)1 << 60;
+    if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
+    const int64_t BH = B * H;
+    const int64_t Np = (N + fa::bwd::BQ - 1) / fa::bwd::BQ * fa::bwd::BQ;
+    const int64_t num_kb = (N + fa::bwd::BKV - 1) / fa::bwd::BKV;
+    if (Np > INT32_MAX / 2 || BH > INT32_MAX || BH > (int64_t)(INT32_MAX / 2) / num_kb) return FA_ERR_INVALID_ARG;
+    if (BH * Np > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
+    sh->BH = BH;
+    sh->Np = Np;
+    sh->num_kb = num_kb;
+    sh->ws_bytes = (size_t)(BH * Np) * (size_t)(d + 2) * sizeof(float);
+    return FA_OK;
+}
+
+template <int D, bool CAUSAL>
+fa_status launch_bwd_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const CUtensorMap& mdo, const CUtensorMap& mdq, const fa::bwd::Params& p, unsigned grid,
+                          int dev, cudaStream_t st)
+{
+    if (prepare_bwd_kernel<D, CAUSAL>(dev) != cudaSuccess) return FA_ERR_CUDA;
+    fa::bwd::fa_bwd_kernel<D, CAUSAL>
+        <<<grid, fa::bwd::NUM_THREADS, fa::bwd::Layout<D>::SMEM_BYTES, st>>>(mq, mk, mv, mdo, mdq, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------- decode
@@ -345,6 +411,95 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                       : launch<128, false>(mq, mk, mv, p, grid, dev, st);
     return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st)
                   : launch<64, false>(mq, mk, mv, p, grid, dev, st);
+}
+
+fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t* bytes)
+{
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    BwdShape sh;
+    const fa_status st = bwd_check(B, H, N, d, &sh);
+    if (st != FA_OK) return st;
+    *bytes = sh.ws_bytes;
+    return FA_OK;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                 void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream)
+{
+    // ---- argument checks (no CUDA call before these pass)
+    if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+    BwdShape sh;
+    const fa_status chk = bwd_check(B, H, N, d, &sh);
+    if (chk != FA_OK) return chk;
+    if (workspace_bytes < sh.ws_bytes) return FA_ERR_INVALID_ARG;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                          reinterpret_cast<uintptr_t>(dout) | reinterpret_cast<uintptr_t>(dq) |
+                          reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv) |
+                          reinterpret_cast<uintptr_t>(workspace);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = sh.BH;
+    const size_t tb = (size_t)(BH * N * d * 2), lb = (size_t)(BH * N * 4);
+    // Outputs and the workspace may overlap no input and no other output.
+    const void* ins[6] = {q, k, v, o, lse, dout};
+    const size_t in_b[6] = {tb, tb, tb, tb, lb, tb};
+    const void* outs[4] = {dq, dk, dv, workspace};
+    const size_t out_b[4] = {tb, tb, tb, sh.ws_bytes};
+    for (int a = 0; a < 4; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_b[a], ins[b], in_b[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 4; ++b)
+            if (overlaps(outs[a], out_b[a], outs[b], out_b[b])) return FA_ERR_INVALID_ARG;
+    }
+
+    // ---- device
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
+    float* const lse2 = static_cast<float*>(workspace);
+    float* const dsum = lse2 + BH * sh.Np;
+    float* const acc = dsum + BH * sh.Np;
+    CUtensorMap mq, mk, mv, mdo, mdq;
+    if (!make_map(&mq, q, BH, N, d, fa::bwd::BQ) || !make_map(&mk, k, BH, N, d, fa::bwd::BKV) ||
+        !make_map(&mv, v, BH, N, d, fa::bwd::BKV) || !make_map(&mdo, dout, BH, N, d, fa::bwd::BQ) ||
+        !make_acc_map(&mdq, acc, BH, sh.Np, d))
+        return FA_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    // 1. D, L * log2 e, zeroed dQ accumulator.
+    const int64_t rows = BH * sh.Np;
+    fa::bwd::fa_bwd_prep_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
+        (int)N, (int)sh.Np, rows);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+
+    // 2. dK, dV and the dQ accumulator.
+    fa::bwd::Params p;
+    p.dk = static_cast<__nv_bfloat16*>(dk);
+    p.dv = static_cast<__nv_bfloat16*>(dv);
+    p.lse2 = lse2;
+    p.dsum = dsum;
+    p.N = (int)N;
+    p.Np = (int)sh.Np;
+    p.num_kb = (int)sh.num_kb;
+    p.num_items = (int)(BH * sh.num_kb);
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.scale = scale;
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    const unsigned grid = (unsigned)std::min<int64_t>((BH * sh.num_kb + 1) / 2, sms);
+    const fa_status ms = causal ? launch_bwd_main<128, true>(mq, mk, mv, mdo, mdq, p, grid, dev, st)
+                                : launch_bwd_main<128, false>(mq, mk, mv, mdo, mdq, p, grid, dev, st);
+    if (ms != FA_OK) return ms;
+
+    // 3. dQ = scale * accumulator, bf16.
+    const int64_t n8 = BH * N * d / 8;
+    fa::bwd::fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
+        acc, static_cast<__nv_bfloat16*>(dq), (int)N, (int)sh.Np, (int)d, n8, scale);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)

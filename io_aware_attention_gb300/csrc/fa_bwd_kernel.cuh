@@ -1,0 +1,635 @@
+// Attention backward for sm_103a: tcgen05 tensor cores + TMEM + TMA.
+//
+// The gradients of O = softmax(scale * Q K^T (+ causal mask)) V for a given
+// dO, with P recomputed tile by tile from the forward's logsumexp L instead of
+// being stored ("Writing and Benchmarking Custom Kernels" §10.3.2):
+//
+//   D_i   = dO_i . O_i                                 (fa_bwd_prep_kernel)
+//   P_ij  = 2^(S_ij * scale * log2 e - L_i * log2 e)   (S = Q K^T recomputed)
+//   dV_j += sum_i P_ij dO_i
+//   dP_ij = dO_i . V_j
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dK_j += scale * sum_i dS_ij Q_i
+//   dQ_i += scale * sum_j dS_ij K_j                    (fp32, added in L2)
+//
+// A work item is BKV = 128 keys of one (batch, head).  The item's K and V
+// stay in shared memory while its query blocks of BQ = 64 rows stream
+// through (under the causal mask only the blocks at or below the diagonal),
+// and dK, dV accumulate in TMEM.  That is the loop order the page describes
+// for the K/V gradient pass (query tiles inner), so dK and dV need no atomics;
+// each step's dQ contribution is added into an fp32 accumulator in global
+// memory with a TMA reduce-add, and fa_bwd_dq_kernel converts it at the end.
+//
+// Everything is computed transposed, keys on the TMEM lanes:
+//   S^T  = K Q^T        (M = 128 keys, N = 64 queries, K = d)     smem x smem
+//   dP^T = V dO^T       (same shape)                              smem x smem
+//   dV  += P^T dO       (M = 128 keys, N = d, K = 64 queries)     TMEM x smem
+//   dK  += dS^T Q       (same shape)                              smem x smem
+//   dQ^T = K^T dS^T     (M = d, N = 64 queries, K = 128 keys)     smem x smem
+// so a thread of the P/dS warps owns one key row and P^T lands in TMEM in
+// the layout the TS-form dV MMA reads as its A operand.  dS^T is written once
+// to shared memory (128 rows of 128 bytes, 128-byte swizzle); the same bytes
+// are the K-major A operand of the dK MMA and the MN-major B operand of the
+// dQ MMA.  K is the MN-major A operand of the dQ MMA (K^T read in place).
+//
+// Warp roles (448 threads):
+//   warps 0-7   P / dS.  Warp w serves keys 32*(w%4) .. +31 (its TMEM lane
+//               quarter) and query columns 32*(w/4) .. +31 of every step.
+//   warps 8-11  dQ: TMEM -> shared staging -> TMA reduce-add into the fp32
+//               accumulator; at the end of an item, the dK / dV epilogue.
+//   warp 12     TMA producer: K, V once per item; Q, dO, L*log2 e and D of
+//               each query block into a ring of stages.
+//   warp 13     MMA issuer (one elected lane); also allocates TMEM.
+//
+// TMEM columns (512): [0,64) S^T buffer 0, [64,128) S^T buffer 1 (P^T as bf16
+// pairs is written over the first 16 columns of each 32-column half of its
+// own buffer), [128,192) dP^T, [192,256) dQ^T, [256,256+d) dV, [384,384+d) dK.
+//
+// MMA order per step g (query block), one issuer: S(g+1), dV(g), dP(g+1),
+// dK(g), dQ(g).  S and dP of the next block are queued before the current
+// block's gradient MMAs, so the tensor pipe has work while the P/dS warps
+// turn S(g+1) into P(g+1).
+//
+// Every wait is bounded in time (see wait_bar); on expiry the CTA records the
+// wait in the device status word, all roles stop, drain their in-flight
+// copies / MMAs and reach the common exit, where TMEM is freed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "fa_fwd_kernel.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int BKV = 128;  // keys per work item (TMEM lanes)
+constexpr int BQ = 64;    // query rows per step
+constexpr int PDS_WARPS = 8;
+constexpr int WARP_DQ0 = 8;  // warps 8..11
+constexpr int WARP_TMA = 12;
+constexpr int WARP_MMA = 13;
+constexpr int NUM_THREADS = 14 * 32;
+constexpr int QSTAGES = 2;
+constexpr uint32_t TM_S0 = 0, TM_S1 = 64, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
+constexpr uint32_t TM_COLS = 512;
+
+struct Params {
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    const float* lse2;  // (B*H, Np): L * log2 e; +inf for rows >= N
+    const float* dsum;  // (B*H, Np): D; 0 for rows >= N
+    int N;
+    int Np;        // query rows rounded up to a multiple of BQ
+    int num_kb;    // key blocks per head
+    int num_items; // B*H*num_kb
+    float scale_log2;
+    float scale;
+    unsigned long long wait_limit_ns;
+};
+
+template <int D>
+struct Layout {
+    static_assert(D == 128, "head size");
+    static constexpr uint32_t KV_BYTES = BKV * D * 2;   // K or V of an item (two 64-column blocks)
+    static constexpr uint32_t KBLK = BKV * 128;         // one 64-column block of K or V (16 KB)
+    static constexpr uint32_t QT_BYTES = BQ * D * 2;    // a Q or dO tile
+    static constexpr uint32_t QBLK = BQ * 128;          // one 64-column block of it (8 KB)
+    static constexpr uint32_t DS_BYTES = BKV * BQ * 2;  // dS^T tile (128 rows x 128 B)
+    static constexpr uint32_t STG_WARP = BQ * 32 * 4;   // one dQ warp's fp32 staging (64 x 32)
+    static constexpr uint32_t ROW_BYTES = 2 * BQ * 4;   // L*log2 e and D of a query block
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
+    static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * QT_BYTES;
+    static constexpr uint32_t OFF_DS = OFF_DO + QSTAGES * QT_BYTES;
+    static constexpr uint32_t OFF_STG = OFF_DS + 2 * DS_BYTES;
+    static constexpr uint32_t OFF_ROW = OFF_STG + 4 * STG_WARP;
+    static constexpr uint32_t OFF_BAR = OFF_ROW + QSTAGES * ROW_BYTES;
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_KVEMPTY = 1;
+    static constexpr int B_QFULL = 2;                 // QSTAGES
+    static constexpr int B_QEMPTY = B_QFULL + QSTAGES;
+    static constexpr int B_SFULL = B_QEMPTY + QSTAGES;  // 2 (per S buffer)
+    static constexpr int B_PFULL = B_SFULL + 2;         // 2
+    static constexpr int B_PFREE = B_PFULL + 2;         // 2
+    static constexpr int B_DPFULL = B_PFREE + 2;
+    static constexpr int B_DPREAD = B_DPFULL + 1;
+    static constexpr int B_DSFULL = B_DPREAD + 1;       // 2 (per dS buffer)
+    static constexpr int B_DSFREE = B_DSFULL + 2;       // 2
+    static constexpr int B_DQFULL = B_DSFREE + 2;
+    static constexpr int B_DQFREE = B_DQFULL + 1;
+    static constexpr int B_ACCFULL = B_DQFREE + 1;
+    static constexpr int B_ACCFREE = B_ACCFULL + 1;
+    static constexpr int B_DRAIN = B_ACCFREE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort
+    static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0 && OFF_DS % 1024 == 0, "swizzled tiles");
+};
+
+// Work item i -> (flattened head, key block).  Within a head the key blocks
+// come light, heavy, light, heavy (kb = M-1, 0, M-2, 1, ...), and a CTA takes
+// both items of a pair (2p, 2p+1): under the causal mask key block kb sees
+// the query blocks from the diagonal on, so every pair costs about the same.
+struct Item {
+    int bh, key0, m0, nq;  // first key, first query block, query blocks
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item item_of(int i, const Params& p)
+{
+    Item it;
+    const int t = i % p.num_kb;
+    const int kb = (t & 1) ? (t >> 1) : (p.num_kb - 1 - (t >> 1));
+    it.bh = i / p.num_kb;
+    it.key0 = kb * BKV;
+    const int nqb = p.Np / BQ;
+    it.m0 = CAUSAL ? it.key0 / BQ : 0;
+    it.nq = nqb - it.m0;
+    return it;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq, const Params p)
+{
+    using L = Layout<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t sbase = ptx::smem_addr(smem_raw);
+    uint8_t* const sgen = smem_raw;
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_status, STATUS_BAD_SMEM);
+        return;
+    }
+    volatile uint32_t* const misc = reinterpret_cast<volatile uint32_t*>(sgen + L::OFF_MISC);
+    volatile uint32_t* const abort_flag = misc + 1;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::OFF_BAR + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint64_t limit = p.wait_limit_ns;
+    const int N = p.N;
+    auto first_item = [&]() -> int { return 2 * (int)blockIdx.x; };
+    auto next_item = [&](int i, int& step) -> int {
+        ++step;
+        return (step & 1) ? i + 1 : i - 1 + 2 * (int)gridDim.x;
+    };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(L::B_KVFULL), 1);
+        ptx::mbar_init(bar(L::B_KVEMPTY), 1);
+        for (int s = 0; s < QSTAGES; ++s) {
+            ptx::mbar_init(bar(L::B_QFULL + s), 1);
+            ptx::mbar_init(bar(L::B_QEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(L::B_SFULL + b), 1);
+            ptx::mbar_init(bar(L::B_PFULL + b), PDS_WARPS);
+            ptx::mbar_init(bar(L::B_PFREE + b), 1);
+            ptx::mbar_init(bar(L::B_DSFULL + b), PDS_WARPS);
+            ptx::mbar_init(bar(L::B_DSFREE + b), 1);
+        }
+        ptx::mbar_init(bar(L::B_DPFULL), 1);
+        ptx::mbar_init(bar(L::B_DPREAD), PDS_WARPS);
+        ptx::mbar_init(bar(L::B_DQFULL), 1);
+        ptx::mbar_init(bar(L::B_DQFREE), 4);
+        ptx::mbar_init(bar(L::B_ACCFULL), 1);
+        ptx::mbar_init(bar(L::B_ACCFREE), 4);
+        ptx::mbar_init(bar(L::B_DRAIN), 1);
+        *abort_flag = 0u;
+        ptx::fence_barrier_init();
+    }
+    if (warp == WARP_TMA && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_do);
+        ptx::prefetch_tensormap(&tm_dq);
+    }
+    if (warp == WARP_MMA) {
+        ptx::tmem_alloc(sbase + L::OFF_MISC, TM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = misc[0];
+
+    if (warp == WARP_TMA) {
+        // ---------------------------------------------------- TMA producer
+        int g = 0, k = 0;
+        bool ok = true;
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const Item it = item_of<CAUSAL>(i, p);
+            if (!(ok = warp_wait_bar(bar(L::B_KVEMPTY), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                     0x1100 + L::B_KVEMPTY)))
+                break;
+            if (ptx::elect_one()) {
+                ptx::mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::KV_BYTES);
+                for (int c = 0; c < D / 64; ++c) {
+                    ptx::tma_load_3d(sbase + L::OFF_K + c * L::KBLK, &tm_k, bar(L::B_KVFULL), c * 64, it.key0, it.bh);
+                    ptx::tma_load_3d(sbase + L::OFF_V + c * L::KBLK, &tm_v, bar(L::B_KVFULL), c * 64, it.key0, it.bh);
+                }
+            }
+            for (int t = 0; ok && t < it.nq; ++t, ++g) {
+                const int s = g % QSTAGES;
+                if (!(ok = warp_wait_bar(bar(L::B_QEMPTY + s), ((uint32_t)(g / QSTAGES) & 1u) ^ 1u, limit,
+                                         abort_flag, 0x1100 + L::B_QEMPTY + s)))
+                    break;
+                if (ptx::elect_one()) {
+                    const int q0 = (it.m0 + t) * BQ;
+                    const uint32_t fb = bar(L::B_QFULL + s);
+                    ptx::mbar_arrive_expect_tx(fb, 2 * L::QT_BYTES + L::ROW_BYTES);
+                    for (int c = 0; c < D / 64; ++c) {
+                        ptx::tma_load_3d(sbase + L::OFF_Q + s * L::QT_BYTES + c * L::QBLK, &tm_q, fb, c * 64, q0, it.bh);
+                        ptx::tma_load_3d(sbase + L::OFF_DO + s * L::QT_BYTES + c * L::QBLK, &tm_do, fb, c * 64, q0,
+                                         it.bh);
+                    }
+                    const int64_t r0 = (int64_t)it.bh * p.Np + q0;
+                    const uint32_t rows = sbase + L::OFF_ROW + s * L::ROW_BYTES;
+                    ptx::bulk_load(rows, p.lse2 + r0, BQ * 4, fb);
+                    ptx::bulk_load(rows + BQ * 4, p.dsum + r0, BQ * 4, fb);
+                }
+            }
+        }
+        // Drain: every copy this warp issued lands before exit.
+        if (k > 0) drain_bar(bar(L::B_KVFULL), (uint32_t)((k - 1) & 1), limit, abort_flag, 0x1180);
+        for (int gg = max(0, g - QSTAGES); gg < g; ++gg)
+            drain_bar(bar(L::B_QFULL + gg % QSTAGES), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag, 0x1181);
+    } else if (warp == WARP_MMA) {
+        // ----------------------------------------------------- MMA issuer
+        constexpr uint32_t ID_S = ptx::idesc_bf16_f32_ab(BKV, BQ, false, false);  // S^T, dP^T
+        constexpr uint32_t ID_G = ptx::idesc_bf16_f32_ab(BKV, D, false, true);    // dV, dK
+        constexpr uint32_t ID_Q = ptx::idesc_bf16_f32_ab(D, BQ, true, true);      // dQ^T
+        // K-major descriptors (rows of 128 B, 8-row groups 1024 B apart).
+        const uint64_t k_kmaj = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+        const uint64_t v_kmaj = ptx::sdesc_sw128(sbase + L::OFF_V, 16, 1024);
+        const uint64_t q_kmaj = ptx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
+        const uint64_t do_kmaj = ptx::sdesc_sw128(sbase + L::OFF_DO, 16, 1024);
+        const uint64_t ds_kmaj = ptx::sdesc_sw128(sbase + L::OFF_DS, 16, 1024);
+        // MN-major descriptors (64-element blocks LBO apart, 8-deep K groups 1024 B apart).
+        const uint64_t k_mn = ptx::sdesc_sw128(sbase + L::OFF_K, L::KBLK, 1024);
+        const uint64_t q_mn = ptx::sdesc_sw128(sbase + L::OFF_Q, L::QBLK, 1024);
+        const uint64_t do_mn = ptx::sdesc_sw128(sbase + L::OFF_DO, L::QBLK, 1024);
+        const uint64_t ds_mn = ptx::sdesc_sw128(sbase + L::OFF_DS, L::QBLK, 1024);
+        auto off = [](uint32_t bytes) -> uint64_t { return (uint64_t)(bytes >> 4); };
+
+        int g = 0, k = 0;
+        bool ok = true;
+        // S^T(g) = K Q(g)^T into S buffer g & 1.
+        auto issue_s = [&](int gg) -> bool {
+            const int s = gg % QSTAGES, b = gg & 1;
+            if (!warp_wait_bar(bar(L::B_QFULL + s), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag,
+                               0x1200 + L::B_QFULL + s))
+                return false;
+            // The buffer held P(gg - 2), read by dV(gg - 2).
+            if (gg >= 2 && !warp_wait_bar(bar(L::B_PFREE + b), (uint32_t)((gg - 2) >> 1) & 1u, limit, abort_flag,
+                                          0x1200 + L::B_PFREE + b))
+                return false;
+            ptx::tc_fence_after_sync();
+            const uint32_t d_tm = tmem + (b ? TM_S1 : TM_S0);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if (ptx::elect_one())
+                    ptx::mma_ss(d_tm, k_kmaj + off((kk >> 2) * L::KBLK + (kk & 3) * 32),
+                                q_kmaj + off(s * L::QT_BYTES + (kk >> 2) * L::QBLK + (kk & 3) * 32), ID_S,
+                                kk > 0 ? 1u : 0u);
+            }
+            if (ptx::elect_one()) ptx::tc_commit(bar(L::B_SFULL + b));
+            return true;
+        };
+        // dP^T(g) = V dO(g)^T (the stage was waited for by issue_s(g)).
+        auto issue_dp = [&](int gg) -> bool {
+            const int s = gg % QSTAGES;
+            // The P/dS warps have read dP(gg - 1).
+            if (gg >= 1 && !warp_wait_bar(bar(L::B_DPREAD), (uint32_t)(gg - 1) & 1u, limit, abort_flag,
+                                          0x1200 + L::B_DPREAD))
+                return false;
+            ptx::tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                if (ptx::elect_one())
+                    ptx::mma_ss(tmem + TM_DP, v_kmaj + off((kk >> 2) * L::KBLK + (kk & 3) * 32),
+                                do_kmaj + off(s * L::QT_BYTES + (kk >> 2) * L::QBLK + (kk & 3) * 32), ID_S,
+                                kk > 0 ? 1u : 0u);
+            }
+            if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DPFULL));
+            return true;
+        };
+
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const Item it = item_of<CAUSAL>(i, p);
+            if (!(ok = warp_wait_bar(bar(L::B_KVFULL), (uint32_t)(k & 1), limit, abort_flag, 0x1200 + L::B_KVFULL)))
+                break;
+            if (!(ok = issue_s(g) && issue_dp(g))) break;
+            for (int t = 0; t < it.nq; ++t, ++g) {
+                const int s = g % QSTAGES, b = g & 1;
+                const bool more = t + 1 < it.nq;
+                if (more && !(ok = issue_s(g + 1))) break;
+                // dV += P^T dO: A = P^T from TMEM (bf16 pairs; queries 16kk.. at
+                // column 32*(kk/2) + 8*(kk%2) of the S buffer), B = dO MN-major.
+                if (t == 0 && !(ok = warp_wait_bar(bar(L::B_ACCFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                                   0x1200 + L::B_ACCFREE)))
+                    break;
+                if (!(ok = warp_wait_bar(bar(L::B_PFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
+                                         0x1200 + L::B_PFULL + b)))
+                    break;
+                ptx::tc_fence_after_sync();
+                const uint32_t p_tm = tmem + (b ? TM_S1 : TM_S0);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk) {
+                    if (ptx::elect_one())
+                        ptx::mma_ts(tmem + TM_DV, p_tm + 32u * (kk >> 1) + 8u * (kk & 1),
+                                    do_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (ptx::elect_one()) ptx::tc_commit(bar(L::B_PFREE + b));
+                if (more && !(ok = issue_dp(g + 1))) break;
+                // dK += dS^T Q: A = dS^T K-major, B = Q MN-major.
+                if (!(ok = warp_wait_bar(bar(L::B_DSFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
+                                         0x1200 + L::B_DSFULL + b)))
+                    break;
+                ptx::tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk) {
+                    if (ptx::elect_one())
+                        ptx::mma_ss(tmem + TM_DK, ds_kmaj + off(b * L::DS_BYTES + kk * 32),
+                                    q_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                // dQ^T = K^T dS^T: A = K MN-major, B = dS^T MN-major.  The dQ
+                // warps have read dQ(g - 1) out of TMEM.
+                if (g >= 1 && !(ok = warp_wait_bar(bar(L::B_DQFREE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
+                                                   0x1200 + L::B_DQFREE)))
+                    break;
+                ptx::tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < BKV / 16; ++kk) {
+                    if (ptx::elect_one())
+                        ptx::mma_ss(tmem + TM_DQ, k_mn + off(kk * 2048), ds_mn + off(b * L::DS_BYTES + kk * 2048),
+                                    ID_Q, kk > 0 ? 1u : 0u);
+                }
+                if (ptx::elect_one()) {
+                    ptx::tc_commit(bar(L::B_DQFULL));
+                    ptx::tc_commit(bar(L::B_DSFREE + b));
+                    ptx::tc_commit(bar(L::B_QEMPTY + s));
+                    if (!more) {
+                        ptx::tc_commit(bar(L::B_ACCFULL));
+                        ptx::tc_commit(bar(L::B_KVEMPTY));
+                    }
+                }
+            }
+        }
+        if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
+        drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x1280);
+    } else if (warp >= WARP_DQ0) {
+        // -------------------------------------------- dQ and the epilogue
+        const int quarter = warp & 3;  // dQ^T lanes = head dims 32*quarter ..; dK/dV lanes = keys
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t stg = sbase + L::OFF_STG + quarter * L::STG_WARP;
+        int g = 0, k = 0;
+        bool ok = true;
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const Item it = item_of<CAUSAL>(i, p);
+            for (int t = 0; t < it.nq; ++t, ++g) {
+                if (!(ok = warp_wait_bar(bar(L::B_DQFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1300 + L::B_DQFULL)))
+                    break;
+                ptx::tc_fence_after_sync();
+                uint32_t a[32], c[32];
+                ptx::tmem_ld32(tmem + lane_off + TM_DQ, a);
+                ptx::tmem_ld32(tmem + lane_off + TM_DQ + 32, c);
+                ptx::tmem_wait_ld(a);
+                ptx::reg_fence(c);
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_DQFREE));
+                // The staging block is free once this warp's previous reduce has read it.
+                if (lane == 0) ptx::tma_store_wait_read();
+                __syncwarp();
+                // Row q of the staging block: the 32 head dims of this warp for query q.
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + q * 128 + lane * 4), "r"(a[q]) : "memory");
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (q + 32) * 128 + lane * 4), "r"(c[q])
+                                 : "memory");
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_reduce_add_3d(&tm_dq, stg, quarter * 32, (it.m0 + t) * BQ, it.bh);
+                    ptx::tma_store_commit();
+                }
+            }
+            if (!ok) break;
+            // Epilogue: dV and scale * dK of this warp's 32 keys, bf16.
+            if (!(ok = warp_wait_bar(bar(L::B_ACCFULL), (uint32_t)k & 1u, limit, abort_flag, 0x1300 + L::B_ACCFULL)))
+                break;
+            ptx::tc_fence_after_sync();
+            const int key = it.key0 + quarter * 32 + lane;
+            const bool key_ok = key < N;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                __nv_bfloat16* const dst = (which ? p.dk : p.dv) + ((int64_t)it.bh * N + key) * D;
+                const float mul = which ? p.scale : 1.0f;
+#pragma unroll
+                for (int ch = 0; ch < D / 32; ++ch) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tmem + lane_off + (which ? TM_DK : TM_DV) + ch * 32, o);
+                    ptx::tmem_wait_ld(o);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        w[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
+                    if (key_ok) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            ptx::st_global_v4(dst + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                }
+            }
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(L::B_ACCFREE));
+        }
+        // Every reduce this warp issued completes before exit.
+        if (lane == 0) ptx::bulk_wait_all();
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ P / dS warps
+        const int quarter = warp & 3;
+        const int half = warp >> 2;          // query columns 32*half .. +31 of a step
+        const int r = quarter * 32 + lane;   // key row in the item == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = p.scale_log2;
+        int g = 0;
+        bool ok = true;
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step)) {
+            const Item it = item_of<CAUSAL>(i, p);
+            const int key = it.key0 + r;
+            const bool key_ok = key < N;
+            for (int t = 0; t < it.nq; ++t, ++g) {
+                const int s = g % QSTAGES, b = g & 1;
+                const int q0 = (it.m0 + t) * BQ + half * 32;  // first query of this thread's columns
+                // The stage's L*log2 e and D rows (TMA-written) are visible once its barrier is seen.
+                if (!(ok = warp_wait_bar(bar(L::B_QFULL + s), (uint32_t)(g / QSTAGES) & 1u, limit, abort_flag,
+                                         0x1400 + L::B_QFULL + s)))
+                    break;
+                if (!(ok = warp_wait_bar(bar(L::B_SFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
+                                         0x1400 + L::B_SFULL + b)))
+                    break;
+                ptx::tc_fence_after_sync();
+                const uint32_t s_tm = tmem + lane_off + (b ? TM_S1 : TM_S0) + 32u * half;
+                uint32_t sv[32];
+                ptx::tmem_ld32(s_tm, sv);
+                const float* const rows = reinterpret_cast<const float*>(sgen + L::OFF_ROW + s * L::ROW_BYTES);
+                const float4* const lrow = reinterpret_cast<const float4*>(rows + half * 32);
+                const float4* const drow = reinterpret_cast<const float4*>(rows + BQ + half * 32);
+                ptx::tmem_wait_ld(sv);
+                // P = 2^(s * scale * log2 e - L * log2 e); masked entries 0.
+                float pf[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 l4 = lrow[c4];
+                    pf[4 * c4 + 0] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 0]), sl2, -l4.x));
+                    pf[4 * c4 + 1] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 1]), sl2, -l4.y));
+                    pf[4 * c4 + 2] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 2]), sl2, -l4.z));
+                    pf[4 * c4 + 3] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 3]), sl2, -l4.w));
+                }
+                if (!key_ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) pf[c] = 0.f;
+                } else if (CAUSAL && q0 < it.key0 + BKV - 1) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (q0 + c < key) pf[c] = 0.f;
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) pk[c] = ptx::pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
+                ptx::tmem_st16(s_tm, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + b));
+
+                if (!(ok = warp_wait_bar(bar(L::B_DPFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1400 + L::B_DPFULL)))
+                    break;
+                ptx::tc_fence_after_sync();
+                uint32_t dp[32];
+                ptx::tmem_ld32(tmem + lane_off + TM_DP + 32u * half, dp);
+                ptx::tmem_wait_ld(dp);
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_DPREAD));
+                // dS = P (dP - D), bf16 pairs.
+                uint32_t dk2[16];
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    const float4 d4 = drow[c4];
+                    const float e0 = pf[4 * c4 + 0] * (__uint_as_float(dp[4 * c4 + 0]) - d4.x);
+                    const float e1 = pf[4 * c4 + 1] * (__uint_as_float(dp[4 * c4 + 1]) - d4.y);
+                    const float e2 = pf[4 * c4 + 2] * (__uint_as_float(dp[4 * c4 + 2]) - d4.z);
+                    const float e3 = pf[4 * c4 + 3] * (__uint_as_float(dp[4 * c4 + 3]) - d4.w);
+                    dk2[2 * c4] = ptx::pack_bf16x2(e0, e1);
+                    dk2[2 * c4 + 1] = ptx::pack_bf16x2(e2, e3);
+                }
+                // dS^T into buffer b (row r, bytes 64*half .. +63, 128-byte
+                // swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7))
+                // once dK / dQ of step g - 2 have read it.
+                if (g >= 2 && !(ok = warp_wait_bar(bar(L::B_DSFREE + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
+                                                   abort_flag, 0x1400 + L::B_DSFREE + b)))
+                    break;
+                const uint32_t row_addr = sbase + L::OFF_DS + b * L::DS_BYTES + (uint32_t)r * 128u;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t chunk = (uint32_t)(half * 4 + u) ^ (uint32_t)(r & 7);
+                    ptx::st_shared_v4(row_addr + chunk * 16u, dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_DSFULL + b));
+            }
+        }
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, TM_COLS);
+    }
+}
+
+// D_i = dO_i . O_i and L_i * log2 e for every row i < Np of every head (rows
+// >= N: D = 0, L * log2 e = +inf, so their recomputed P is 0), and the fp32
+// dQ accumulator zeroed.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                       const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dsum,
+                       float* __restrict__ dq_acc, int N, int Np, int64_t rows)
+{
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int64_t bh = row / Np;
+    const int i = (int)(row - bh * Np);
+    constexpr int E = D / 32;  // elements per lane
+    float acc = 0.f;
+    if (i < N) {
+        const int64_t base = (bh * N + i) * D + lane * E;
+        if constexpr (E == 4) {
+            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+            const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
+            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
+            const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
+            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
+            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
+            acc = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+        } else {
+            const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
+            const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base);
+            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
+            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
+            acc = a0.x * b0.x + a0.y * b0.y;
+        }
+    }
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (lane == 0) {
+        dsum[row] = i < N ? acc : 0.f;
+        lse2[row] = i < N ? lse[bh * N + i] * 1.4426950408889634074f : __int_as_float(0x7f800000);
+    }
+    float4* const z = reinterpret_cast<float4*>(dq_acc + row * D);
+    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = bf16(scale * accumulator) for rows < N.  Each thread converts 8
+// consecutive elements.
+__global__ void __launch_bounds__(256)
+    fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Np, int D,
+                     int64_t n8, float scale)
+{
+    const int64_t e8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e8 >= n8) return;
+    const int64_t e = e8 * 8;
+    const int64_t row = e / D;  // bh * N + i
+    const int col = (int)(e - row * D);
+    const int64_t bh = row / N;
+    const int64_t i = row - bh * N;
+    const float4* const src = reinterpret_cast<const float4*>(dq_acc + (bh * Np + i) * D + col);
+    const float4 a = src[0], b = src[1];
+    uint4 w;
+    w.x = ptx::pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = ptx::pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = ptx::pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = ptx::pack_bf16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + e) = w;
+}
+
+}  // namespace bwd
+}  // namespace fa

@@ -114,3 +114,40 @@ def test_decode_workspace_query_checks_arguments(lib):
     out = ctypes.c_size_t(0)
     assert lib.fa_decode_workspace_bytes(1, 1, 9, 64, 128, 0, ctypes.byref(out)) == 2
     assert lib.fa_decode_workspace_bytes(1, 1, 1, 64, 128, 0, None) == 1
+
+
+def call_bwd(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, do=6 * P, dq=7 * P, dk=8 * P, dv=9 * P, B=1, H=1,
+             N=16, d=128, causal=0, scale=0.125, ws=10 * P, ws_bytes=1 << 20):
+    vp = ctypes.c_void_p
+    return lib.fa_bwd(vp(q), vp(k), vp(v), vp(o), vp(lse), vp(do), vp(dq), vp(dk), vp(dv), B, H, N, d, causal,
+                      scale, vp(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(q=0), 1), (dict(o=0), 1), (dict(lse=0), 1), (dict(do=0), 1), (dict(dq=0), 1), (dict(dv=0), 1),
+    (dict(ws=0), 1), (dict(B=0), 1), (dict(N=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(d=64), 2), (dict(d=96), 2),                 # head size
+    (dict(do=6 * P + 8), 2), (dict(dk=8 * P + 2), 2), (dict(lse=5 * P + 2), 2), (dict(ws=10 * P + 4), 2),
+    (dict(ws_bytes=64 * 130 * 4 - 16), 1),            # workspace one row short
+    (dict(dq=P), 1),                                  # dq aliases q
+    (dict(dk=6 * P + 16), 1),                         # dk overlaps dO
+    (dict(dv=8 * P + 512), 1),                        # dv overlaps dk
+    (dict(ws=9 * P + 256), 1),                        # workspace overlaps dv
+    (dict(lse=7 * P + 64), 1),                        # dq overlaps lse
+    (dict(B=1 << 40, H=1 << 20), 1),                  # element count overflows
+])
+def test_bad_bwd_arguments_are_rejected(lib, kw, status):
+    assert call_bwd(lib, **kw) == status
+
+
+def test_bwd_workspace_bytes(lib):
+    out = ctypes.c_size_t(0)
+    # rows rounded up to 64 per head; two fp32 row vectors and the fp32 dQ accumulator
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100, 128, ctypes.byref(out)) == 0
+    assert out.value == 2 * 3 * 128 * (128 + 2) * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 128, ctypes.byref(out)) == 0
+    assert out.value == 64 * 130 * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 64, ctypes.byref(out)) == 2
+    assert lib.fa_bwd_workspace_bytes(1, 1, 0, 128, ctypes.byref(out)) == 1
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 128, None) == 1
