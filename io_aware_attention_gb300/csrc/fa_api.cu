@@ -157,7 +157,8 @@ fa_status bwd_check(int64_t B, int64_t H, int64_t N, int64_t d, BwdShape* sh)
     const int64_t BH = B * H;
     const int64_t Np = (N + fa::bwd::BQ - 1) / fa::bwd::BQ * fa::bwd::BQ;
     const int64_t num_kb = (N + fa::bwd::BKV - 1) / fa::bwd::BKV;
-    if (Np > INT32_MAX / 2 || BH > INT32_MAX || BH > (int64_t)(INT32_MAX / 2) / num_kb) return FA_ERR_INVALID_ARG;
+    // BH is the dQ conversion's grid.y; items are int
+    if (Np > INT32_MAX / 2 || BH > 65535 || BH > (int64_t)(INT32_MAX / 2) / num_kb) return FA_ERR_INVALID_ARG;
     if (BH * Np > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
     sh->BH = BH;
     sh->Np = Np;
@@ -483,6 +484,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.dv = static_cast<__nv_bfloat16*>(dv);
     p.lse2 = lse2;
     p.dsum = dsum;
+    p.dq_acc = acc;
     p.N = (int)N;
     p.Np = (int)sh.Np;
     p.num_kb = (int)sh.num_kb;

@@ -18,7 +18,8 @@
 // and dK, dV accumulate in TMEM.  That is the loop order the page describes
 // for the K/V gradient pass (query tiles inner), so dK and dV need no atomics;
 // each step's dQ contribution is added into an fp32 accumulator in global
-// memory with a TMA reduce-add, and fa_bwd_dq_kernel converts it at the end.
+// memory with a TMA reduce-add (the add happens in L2), and fa_bwd_dq_kernel
+// converts it at the end.
 //
 // Everything is computed transposed, keys on the TMEM lanes:
 //   S^T  = K Q^T        (M = 128 keys, N = 64 queries, K = d)     smem x smem
@@ -35,24 +36,49 @@
 // Warp roles (448 threads):
 //   warps 0-7   P / dS.  Warp w serves keys 32*(w%4) .. +31 (its TMEM lane
 //               quarter) and query columns 32*(w/4) .. +31 of every step.
-//   warps 8-11  dQ: TMEM -> shared staging -> TMA reduce-add into the fp32
-//               accumulator; at the end of an item, the dK / dV epilogue.
-//   warp 12     TMA producer: K, V once per item; Q, dO, L*log2 e and D of
-//               each query block into a ring of stages.
+//   warps 8-11  dQ: TMEM -> registers -> a shared-memory staging block ->
+//               TMA reduce-add into the fp32 accumulator; at the end of an
+//               item, the dK / dV epilogue.
+//   warp 12     TMA producer: K, V once per item; Q and dO of each query
+//               block into a ring of stages.
 //   warp 13     MMA issuer (one elected lane); also allocates TMEM.
 //
 // TMEM columns (512): [0,64) S^T buffer 0, [64,128) S^T buffer 1 (P^T as bf16
 // pairs is written over the first 16 columns of each 32-column half of its
 // own buffer), [128,192) dP^T, [192,256) dQ^T, [256,256+d) dV, [384,384+d) dK.
 //
-// MMA order per step g (query block), one issuer: S(g+1), dV(g), dP(g+1),
-// dK(g), dQ(g).  S and dP of the next block are queued before the current
-// block's gradient MMAs, so the tensor pipe has work while the P/dS warps
-// turn S(g+1) into P(g+1).
+// Shared memory is the tight resource.  An M = 128 MMA with both operands
+// in shared memory reads them at the full 128 bytes per cycle of the SM (a
+// 64-column MMA takes 48 cycles instead of 32), and while the tensor core
+// does so every other shared-memory access queues behind it -- including
+// mbarrier waits, which then take ~1000 cycles even on a completed phase.
+// Hence:
+//   - warps signal the MMA issuer through hardware named barriers (no shared
+//     memory); mbarriers are left for what only they can carry: TMA byte
+//     counts and MMA completion (tcgen05.commit);
+//   - the issue order makes most completions implied: per step g
+//         dV(g); [dP(g) read] S(g+1), dP(g+1); [dS(g) ready] dK(g); dQ(g)
+//     The dP-read signal means dP(g) is complete, hence every MMA issued
+//     before it, among them dV(g-1), the last reader of S(g+1)'s buffer;
+//     dP(g+2) completing means dK(g) and dQ(g), the readers of dS buffer
+//     g & 1, are complete;
+//   - the P/dS warps take L*log2 e and D from global memory (L1/L2), loaded
+//     at the top of a step, not from shared memory;
+//   - the dQ contribution leaves through one bulk TMA reduce-add per warp and
+//     step.  Per-element atomics from registers were tried: their thousands
+//     of memory requests per step stall every warp's barrier operations
+//     behind them (about 2000 cycles a step, against 150 for the staging
+//     round trip);
+//   - the Q/dO ring is three stages deep, released as soon as dK(g), its
+//     last reader, is done.
 //
-// Every wait is bounded in time (see wait_bar); on expiry the CTA records the
-// wait in the device status word, all roles stop, drain their in-flight
-// copies / MMAs and reach the common exit, where TMEM is freed.
+// Named barriers are counted, not timed: every role executes each of its
+// bar.arrive / bar.sync once per step (or item) whatever happened, so the
+// counts always match.  mbarrier waits are bounded in time (see wait_bar);
+// on expiry the CTA records the wait in the device status word and raises an
+// abort flag, after which the roles keep walking their loops (skipping the
+// work, still meeting the named barriers), drain in-flight copies / MMAs and
+// reach the common exit, where TMEM is freed.
 #pragma once
 
 #include <cuda.h>
@@ -72,15 +98,32 @@ constexpr int WARP_DQ0 = 8;  // warps 8..11
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA = 13;
 constexpr int NUM_THREADS = 14 * 32;
-constexpr int QSTAGES = 2;
+constexpr int QSTAGES = 3;
 constexpr uint32_t TM_S0 = 0, TM_S1 = 64, TM_DP = 128, TM_DQ = 192, TM_DV = 256, TM_DK = 384;
 constexpr uint32_t TM_COLS = 512;
+
+// Named barriers (0 is __syncthreads).  P/dS warps -> issuer: 256 + 32
+// threads; dQ warps -> issuer: 128 + 32.  P_READY and DS_READY alternate
+// between two ids by step parity: the P/dS warps may run one step ahead.
+constexpr uint32_t NB_P_READY = 1;    // + (g & 1): P(g) in TMEM
+constexpr uint32_t NB_DS_READY = 3;   // + (g & 1): dS(g) in shared memory
+constexpr uint32_t NB_DP_READ = 5;    // dP(g) read out of TMEM (so dP(g) is complete)
+constexpr uint32_t NB_DQ_READ = 6;    // dQ(g) read out of TMEM
+constexpr uint32_t NB_ACC_READ = 7;   // dK, dV of an item read out of TMEM
+constexpr uint32_t NB_PDS_COUNT = 32 * PDS_WARPS + 32;
+constexpr uint32_t NB_DQ_COUNT = 32 * 4 + 32;
+
+__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
 struct Params {
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     const float* lse2;  // (B*H, Np): L * log2 e; +inf for rows >= N
     const float* dsum;  // (B*H, Np): D; 0 for rows >= N
+    float* dq_acc;      // (B*H, Np, d): fp32 dQ / scale
     int N;
     int Np;        // query rows rounded up to a multiple of BQ
     int num_kb;    // key blocks per head
@@ -99,31 +142,22 @@ struct Layout {
     static constexpr uint32_t QBLK = BQ * 128;          // one 64-column block of it (8 KB)
     static constexpr uint32_t DS_BYTES = BKV * BQ * 2;  // dS^T tile (128 rows x 128 B)
     static constexpr uint32_t STG_WARP = BQ * 32 * 4;   // one dQ warp's fp32 staging (64 x 32)
-    static constexpr uint32_t ROW_BYTES = 2 * BQ * 4;   // L*log2 e and D of a query block
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
     static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
     static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * QT_BYTES;
     static constexpr uint32_t OFF_DS = OFF_DO + QSTAGES * QT_BYTES;
     static constexpr uint32_t OFF_STG = OFF_DS + 2 * DS_BYTES;
-    static constexpr uint32_t OFF_ROW = OFF_STG + 4 * STG_WARP;
-    static constexpr uint32_t OFF_BAR = OFF_ROW + QSTAGES * ROW_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_STG + 4 * STG_WARP;
     static constexpr int B_KVFULL = 0;
     static constexpr int B_KVEMPTY = 1;
-    static constexpr int B_QFULL = 2;                 // QSTAGES
-    static constexpr int B_QEMPTY = B_QFULL + QSTAGES;
+    static constexpr int B_QFULL = 2;                   // QSTAGES
+    static constexpr int B_QEMPTY = B_QFULL + QSTAGES;  // QSTAGES
     static constexpr int B_SFULL = B_QEMPTY + QSTAGES;  // 2 (per S buffer)
-    static constexpr int B_PFULL = B_SFULL + 2;         // 2
-    static constexpr int B_PFREE = B_PFULL + 2;         // 2
-    static constexpr int B_DPFULL = B_PFREE + 2;
-    static constexpr int B_DPREAD = B_DPFULL + 1;
-    static constexpr int B_DSFULL = B_DPREAD + 1;       // 2 (per dS buffer)
-    static constexpr int B_DSFREE = B_DSFULL + 2;       // 2
-    static constexpr int B_DQFULL = B_DSFREE + 2;
-    static constexpr int B_DQFREE = B_DQFULL + 1;
-    static constexpr int B_ACCFULL = B_DQFREE + 1;
-    static constexpr int B_ACCFREE = B_ACCFULL + 1;
-    static constexpr int B_DRAIN = B_ACCFREE + 1;
+    static constexpr int B_DPFULL = B_SFULL + 2;
+    static constexpr int B_DQFULL = B_DPFULL + 1;
+    static constexpr int B_ACCFULL = B_DQFULL + 1;
+    static constexpr int B_DRAIN = B_ACCFULL + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
@@ -188,19 +222,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(L::B_QFULL + s), 1);
             ptx::mbar_init(bar(L::B_QEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar(L::B_SFULL + b), 1);
-            ptx::mbar_init(bar(L::B_PFULL + b), PDS_WARPS);
-            ptx::mbar_init(bar(L::B_PFREE + b), 1);
-            ptx::mbar_init(bar(L::B_DSFULL + b), PDS_WARPS);
-            ptx::mbar_init(bar(L::B_DSFREE + b), 1);
-        }
+        ptx::mbar_init(bar(L::B_SFULL), 1);
+        ptx::mbar_init(bar(L::B_SFULL + 1), 1);
         ptx::mbar_init(bar(L::B_DPFULL), 1);
-        ptx::mbar_init(bar(L::B_DPREAD), PDS_WARPS);
         ptx::mbar_init(bar(L::B_DQFULL), 1);
-        ptx::mbar_init(bar(L::B_DQFREE), 4);
         ptx::mbar_init(bar(L::B_ACCFULL), 1);
-        ptx::mbar_init(bar(L::B_ACCFREE), 4);
         ptx::mbar_init(bar(L::B_DRAIN), 1);
         *abort_flag = 0u;
         ptx::fence_barrier_init();
@@ -245,16 +271,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (ptx::elect_one()) {
                     const int q0 = (it.m0 + t) * BQ;
                     const uint32_t fb = bar(L::B_QFULL + s);
-                    ptx::mbar_arrive_expect_tx(fb, 2 * L::QT_BYTES + L::ROW_BYTES);
+                    ptx::mbar_arrive_expect_tx(fb, 2 * L::QT_BYTES);
                     for (int c = 0; c < D / 64; ++c) {
                         ptx::tma_load_3d(sbase + L::OFF_Q + s * L::QT_BYTES + c * L::QBLK, &tm_q, fb, c * 64, q0, it.bh);
                         ptx::tma_load_3d(sbase + L::OFF_DO + s * L::QT_BYTES + c * L::QBLK, &tm_do, fb, c * 64, q0,
                                          it.bh);
                     }
-                    const int64_t r0 = (int64_t)it.bh * p.Np + q0;
-                    const uint32_t rows = sbase + L::OFF_ROW + s * L::ROW_BYTES;
-                    ptx::bulk_load(rows, p.lse2 + r0, BQ * 4, fb);
-                    ptx::bulk_load(rows + BQ * 4, p.dsum + r0, BQ * 4, fb);
                 }
             }
         }
@@ -280,18 +302,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t ds_mn = ptx::sdesc_sw128(sbase + L::OFF_DS, L::QBLK, 1024);
         auto off = [](uint32_t bytes) -> uint64_t { return (uint64_t)(bytes >> 4); };
 
-        int g = 0, k = 0;
         bool ok = true;
-        // S^T(g) = K Q(g)^T into S buffer g & 1.
-        auto issue_s = [&](int gg) -> bool {
+        // S^T(g) = K Q(g)^T into S buffer g & 1, then dP^T(g) = V dO(g)^T.
+        // The caller has met the dP-read barrier of step g - 1, so every MMA
+        // issued before dP(g-1) -- dV(g-2), the last reader of the S buffer --
+        // is complete, and dP(g-1) has been read out.
+        auto issue_s_dp = [&](int gg) {
             const int s = gg % QSTAGES, b = gg & 1;
-            if (!warp_wait_bar(bar(L::B_QFULL + s), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag,
-                               0x1200 + L::B_QFULL + s))
-                return false;
-            // The buffer held P(gg - 2), read by dV(gg - 2).
-            if (gg >= 2 && !warp_wait_bar(bar(L::B_PFREE + b), (uint32_t)((gg - 2) >> 1) & 1u, limit, abort_flag,
-                                          0x1200 + L::B_PFREE + b))
-                return false;
+            if (ok) ok = warp_wait_bar(bar(L::B_QFULL + s), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag,
+                                       0x1200 + L::B_QFULL + s);
+            if (!ok) return;
             ptx::tc_fence_after_sync();
             const uint32_t d_tm = tmem + (b ? TM_S1 : TM_S0);
 #pragma unroll
@@ -302,16 +322,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 kk > 0 ? 1u : 0u);
             }
             if (ptx::elect_one()) ptx::tc_commit(bar(L::B_SFULL + b));
-            return true;
-        };
-        // dP^T(g) = V dO(g)^T (the stage was waited for by issue_s(g)).
-        auto issue_dp = [&](int gg) -> bool {
-            const int s = gg % QSTAGES;
-            // The P/dS warps have read dP(gg - 1).
-            if (gg >= 1 && !warp_wait_bar(bar(L::B_DPREAD), (uint32_t)(gg - 1) & 1u, limit, abort_flag,
-                                          0x1200 + L::B_DPREAD))
-                return false;
-            ptx::tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 if (ptx::elect_one())
@@ -320,70 +330,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 kk > 0 ? 1u : 0u);
             }
             if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DPFULL));
-            return true;
         };
 
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+        int g = 0, k = 0;
+        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const Item it = item_of<CAUSAL>(i, p);
-            if (!(ok = warp_wait_bar(bar(L::B_KVFULL), (uint32_t)(k & 1), limit, abort_flag, 0x1200 + L::B_KVFULL)))
-                break;
-            if (!(ok = issue_s(g) && issue_dp(g))) break;
+            if (ok) ok = warp_wait_bar(bar(L::B_KVFULL), (uint32_t)(k & 1), limit, abort_flag, 0x1200 + L::B_KVFULL);
+            if (g >= 1) ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);  // dP(g-1) read
+            issue_s_dp(g);
             for (int t = 0; t < it.nq; ++t, ++g) {
                 const int s = g % QSTAGES, b = g & 1;
                 const bool more = t + 1 < it.nq;
-                if (more && !(ok = issue_s(g + 1))) break;
                 // dV += P^T dO: A = P^T from TMEM (bf16 pairs; queries 16kk.. at
                 // column 32*(kk/2) + 8*(kk%2) of the S buffer), B = dO MN-major.
-                if (t == 0 && !(ok = warp_wait_bar(bar(L::B_ACCFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
-                                                   0x1200 + L::B_ACCFREE)))
-                    break;
-                if (!(ok = warp_wait_bar(bar(L::B_PFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
-                                         0x1200 + L::B_PFULL + b)))
-                    break;
-                ptx::tc_fence_after_sync();
-                const uint32_t p_tm = tmem + (b ? TM_S1 : TM_S0);
+                // The first of an item overwrites dV: the epilogue has read it.
+                if (t == 0 && k > 0) ptx::named_barrier_sync(NB_ACC_READ, NB_DQ_COUNT);
+                ptx::named_barrier_sync(NB_P_READY + (uint32_t)b, NB_PDS_COUNT);
+                if (ok) {
+                    ptx::tc_fence_after_sync();
+                    const uint32_t p_tm = tmem + (b ? TM_S1 : TM_S0);
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk) {
-                    if (ptx::elect_one())
-                        ptx::mma_ts(tmem + TM_DV, p_tm + 32u * (kk >> 1) + 8u * (kk & 1),
-                                    do_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        if (ptx::elect_one())
+                            ptx::mma_ts(tmem + TM_DV, p_tm + 32u * (kk >> 1) + 8u * (kk & 1),
+                                        do_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
-                if (ptx::elect_one()) ptx::tc_commit(bar(L::B_PFREE + b));
-                if (more && !(ok = issue_dp(g + 1))) break;
+                if (more) {
+                    ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);  // dP(g) read
+                    issue_s_dp(g + 1);
+                }
                 // dK += dS^T Q: A = dS^T K-major, B = Q MN-major.
-                if (!(ok = warp_wait_bar(bar(L::B_DSFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
-                                         0x1200 + L::B_DSFULL + b)))
-                    break;
-                ptx::tc_fence_after_sync();
+                ptx::named_barrier_sync(NB_DS_READY + (uint32_t)b, NB_PDS_COUNT);
+                if (ok) {
+                    ptx::tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk) {
-                    if (ptx::elect_one())
-                        ptx::mma_ss(tmem + TM_DK, ds_kmaj + off(b * L::DS_BYTES + kk * 32),
-                                    q_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        if (ptx::elect_one())
+                            ptx::mma_ss(tmem + TM_DK, ds_kmaj + off(b * L::DS_BYTES + kk * 32),
+                                        q_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    // dK(g) is the stage's last reader (S, dP, dV came before it).
+                    if (ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY + s));
                 }
-                // dQ^T = K^T dS^T: A = K MN-major, B = dS^T MN-major.  The dQ
-                // warps have read dQ(g - 1) out of TMEM.
-                if (g >= 1 && !(ok = warp_wait_bar(bar(L::B_DQFREE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
-                                                   0x1200 + L::B_DQFREE)))
-                    break;
-                ptx::tc_fence_after_sync();
+                // dQ^T = K^T dS^T: A = K MN-major, B = dS^T MN-major, once the
+                // dQ warps have read dQ(g - 1) out of TMEM.
+                if (g >= 1) ptx::named_barrier_sync(NB_DQ_READ, NB_DQ_COUNT);
+                if (ok) {
+                    ptx::tc_fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < BKV / 16; ++kk) {
-                    if (ptx::elect_one())
-                        ptx::mma_ss(tmem + TM_DQ, k_mn + off(kk * 2048), ds_mn + off(b * L::DS_BYTES + kk * 2048),
-                                    ID_Q, kk > 0 ? 1u : 0u);
-                }
-                if (ptx::elect_one()) {
-                    ptx::tc_commit(bar(L::B_DQFULL));
-                    ptx::tc_commit(bar(L::B_DSFREE + b));
-                    ptx::tc_commit(bar(L::B_QEMPTY + s));
-                    if (!more) {
-                        ptx::tc_commit(bar(L::B_ACCFULL));
-                        ptx::tc_commit(bar(L::B_KVEMPTY));
+                    for (int kk = 0; kk < BKV / 16; ++kk) {
+                        if (ptx::elect_one())
+                            ptx::mma_ss(tmem + TM_DQ, k_mn + off(kk * 2048), ds_mn + off(b * L::DS_BYTES + kk * 2048),
+                                        ID_Q, kk > 0 ? 1u : 0u);
+                    }
+                    if (ptx::elect_one()) {
+                        ptx::tc_commit(bar(L::B_DQFULL));
+                        if (!more) {
+                            ptx::tc_commit(bar(L::B_ACCFULL));
+                            ptx::tc_commit(bar(L::B_KVEMPTY));
+                        }
                     }
                 }
             }
         }
+        // The last step's signals, so that every named barrier completes.
+        if (g >= 1) {
+            ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);
+            ptx::named_barrier_sync(NB_DQ_READ, NB_DQ_COUNT);
+        }
+        if (k >= 1) ptx::named_barrier_sync(NB_ACC_READ, NB_DQ_COUNT);
         if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
         drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x1280);
     } else if (warp >= WARP_DQ0) {
@@ -393,67 +409,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t stg = sbase + L::OFF_STG + quarter * L::STG_WARP;
         int g = 0, k = 0;
         bool ok = true;
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const Item it = item_of<CAUSAL>(i, p);
             for (int t = 0; t < it.nq; ++t, ++g) {
-                if (!(ok = warp_wait_bar(bar(L::B_DQFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1300 + L::B_DQFULL)))
-                    break;
-                ptx::tc_fence_after_sync();
-                uint32_t a[32], c[32];
-                ptx::tmem_ld32(tmem + lane_off + TM_DQ, a);
-                ptx::tmem_ld32(tmem + lane_off + TM_DQ + 32, c);
-                ptx::tmem_wait_ld(a);
-                ptx::reg_fence(c);
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_DQFREE));
-                // The staging block is free once this warp's previous reduce has read it.
-                if (lane == 0) ptx::tma_store_wait_read();
-                __syncwarp();
-                // Row q of the staging block: the 32 head dims of this warp for query q.
+                if (ok) ok = warp_wait_bar(bar(L::B_DQFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1300 + L::B_DQFULL);
+                if (ok) {
+                    uint32_t a[32], c[32];
+                    ptx::tc_fence_after_sync();
+                    ptx::tmem_ld32(tmem + lane_off + TM_DQ, a);
+                    ptx::tmem_ld32(tmem + lane_off + TM_DQ + 32, c);
+                    ptx::tmem_wait_ld(a);
+                    ptx::reg_fence(c);
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    nb_arrive(NB_DQ_READ, NB_DQ_COUNT);
+                    // The staging block is free once this warp's previous reduce
+                    // has read it.  Row q holds this warp's 32 head dims of query q.
+                    if (lane == 0) ptx::tma_store_wait_read();
+                    __syncwarp();
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + q * 128 + lane * 4), "r"(a[q]) : "memory");
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (q + 32) * 128 + lane * 4), "r"(c[q])
-                                 : "memory");
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_reduce_add_3d(&tm_dq, stg, quarter * 32, (it.m0 + t) * BQ, it.bh);
-                    ptx::tma_store_commit();
+                    for (int q = 0; q < 32; ++q) {
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + q * 128 + lane * 4), "r"(a[q]) : "memory");
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(stg + (q + 32) * 128 + lane * 4), "r"(c[q])
+                                     : "memory");
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_reduce_add_3d(&tm_dq, stg, quarter * 32, (it.m0 + t) * BQ, it.bh);
+                        ptx::tma_store_commit();
+                    }
+                } else {
+                    __syncwarp();
+                    nb_arrive(NB_DQ_READ, NB_DQ_COUNT);
                 }
             }
-            if (!ok) break;
             // Epilogue: dV and scale * dK of this warp's 32 keys, bf16.
-            if (!(ok = warp_wait_bar(bar(L::B_ACCFULL), (uint32_t)k & 1u, limit, abort_flag, 0x1300 + L::B_ACCFULL)))
-                break;
-            ptx::tc_fence_after_sync();
-            const int key = it.key0 + quarter * 32 + lane;
-            const bool key_ok = key < N;
+            if (ok) ok = warp_wait_bar(bar(L::B_ACCFULL), (uint32_t)k & 1u, limit, abort_flag, 0x1300 + L::B_ACCFULL);
+            if (ok) {
+                ptx::tc_fence_after_sync();
+                const int key = it.key0 + quarter * 32 + lane;
+                const bool key_ok = key < N;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                __nv_bfloat16* const dst = (which ? p.dk : p.dv) + ((int64_t)it.bh * N + key) * D;
-                const float mul = which ? p.scale : 1.0f;
+                for (int which = 0; which < 2; ++which) {
+                    __nv_bfloat16* const dst = (which ? p.dk : p.dv) + ((int64_t)it.bh * N + key) * D;
+                    const float mul = which ? p.scale : 1.0f;
 #pragma unroll
-                for (int ch = 0; ch < D / 32; ++ch) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tmem + lane_off + (which ? TM_DK : TM_DV) + ch * 32, o);
-                    ptx::tmem_wait_ld(o);
-                    uint32_t w[16];
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(tmem + lane_off + (which ? TM_DK : TM_DV) + ch * 32, o);
+                        ptx::tmem_wait_ld(o);
+                        uint32_t w[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        w[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
-                    if (key_ok) {
+                        for (int c = 0; c < 16; ++c)
+                            w[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
+                        if (key_ok) {
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            ptx::st_global_v4(dst + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                            for (int u = 0; u < 4; ++u)
+                                ptx::st_global_v4(dst + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                  w[4 * u + 3]);
+                        }
                     }
                 }
+                ptx::tc_fence_before_sync();
             }
-            ptx::tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(L::B_ACCFREE));
+            nb_arrive(NB_ACC_READ, NB_DQ_COUNT);
         }
         // Every reduce this warp issued completes before exit.
         if (lane == 0) ptx::bulk_wait_all();
@@ -467,91 +488,100 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float sl2 = p.scale_log2;
         int g = 0;
         bool ok = true;
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step)) {
+        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
             const Item it = item_of<CAUSAL>(i, p);
             const int key = it.key0 + r;
             const bool key_ok = key < N;
             for (int t = 0; t < it.nq; ++t, ++g) {
-                const int s = g % QSTAGES, b = g & 1;
+                const int b = g & 1;
                 const int q0 = (it.m0 + t) * BQ + half * 32;  // first query of this thread's columns
-                // The stage's L*log2 e and D rows (TMA-written) are visible once its barrier is seen.
-                if (!(ok = warp_wait_bar(bar(L::B_QFULL + s), (uint32_t)(g / QSTAGES) & 1u, limit, abort_flag,
-                                         0x1400 + L::B_QFULL + s)))
-                    break;
-                if (!(ok = warp_wait_bar(bar(L::B_SFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
-                                         0x1400 + L::B_SFULL + b)))
-                    break;
-                ptx::tc_fence_after_sync();
-                const uint32_t s_tm = tmem + lane_off + (b ? TM_S1 : TM_S0) + 32u * half;
-                uint32_t sv[32];
-                ptx::tmem_ld32(s_tm, sv);
-                const float* const rows = reinterpret_cast<const float*>(sgen + L::OFF_ROW + s * L::ROW_BYTES);
-                const float4* const lrow = reinterpret_cast<const float4*>(rows + half * 32);
-                const float4* const drow = reinterpret_cast<const float4*>(rows + BQ + half * 32);
-                ptx::tmem_wait_ld(sv);
-                // P = 2^(s * scale * log2 e - L * log2 e); masked entries 0.
-                float pf[32];
+                // L*log2 e and D of this thread's 32 queries, loaded before the waits.
+                const float4* const lrow = reinterpret_cast<const float4*>(p.lse2 + (int64_t)it.bh * p.Np + q0);
+                const float4* const drow = reinterpret_cast<const float4*>(p.dsum + (int64_t)it.bh * p.Np + q0);
+                float4 l4[8], d4[8];
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const float4 l4 = lrow[c4];
-                    pf[4 * c4 + 0] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 0]), sl2, -l4.x));
-                    pf[4 * c4 + 1] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 1]), sl2, -l4.y));
-                    pf[4 * c4 + 2] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 2]), sl2, -l4.z));
-                    pf[4 * c4 + 3] = ptx::ex2(fmaf(__uint_as_float(sv[4 * c4 + 3]), sl2, -l4.w));
-                }
-                if (!key_ok) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) pf[c] = 0.f;
-                } else if (CAUSAL && q0 < it.key0 + BKV - 1) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (q0 + c < key) pf[c] = 0.f;
-                }
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) pk[c] = ptx::pack_bf16x2(pf[2 * c], pf[2 * c + 1]);
-                ptx::tmem_st16(s_tm, pk);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + b));
+                for (int c4 = 0; c4 < 8; ++c4) l4[c4] = __ldg(lrow + c4);
 
-                if (!(ok = warp_wait_bar(bar(L::B_DPFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1400 + L::B_DPFULL)))
-                    break;
-                ptx::tc_fence_after_sync();
+                if (ok) ok = warp_wait_bar(bar(L::B_SFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
+                                           0x1400 + L::B_SFULL + b);
+                const uint32_t s_tm = tmem + lane_off + (b ? TM_S1 : TM_S0) + 32u * half;
+                // The scores, then (in place) P as fp32 bit patterns.
+                uint32_t pv[32];
+                if (!ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) pv[c] = 0u;
+                } else {
+                    ptx::tc_fence_after_sync();
+                    ptx::tmem_ld32(s_tm, pv);
+                    ptx::tmem_wait_ld(pv);
+                    // P = 2^(s * scale * log2 e - L * log2 e); masked entries 0.
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        pv[4 * c4 + 0] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pv[4 * c4 + 0]), sl2, -l4[c4].x)));
+                        pv[4 * c4 + 1] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pv[4 * c4 + 1]), sl2, -l4[c4].y)));
+                        pv[4 * c4 + 2] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pv[4 * c4 + 2]), sl2, -l4[c4].z)));
+                        pv[4 * c4 + 3] = __float_as_uint(ptx::ex2(fmaf(__uint_as_float(pv[4 * c4 + 3]), sl2, -l4[c4].w)));
+                    }
+                    if (!key_ok) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) pv[c] = 0u;
+                    } else if (CAUSAL && q0 < it.key0 + BKV - 1) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            if (q0 + c < key) pv[c] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) pk[c] = ptx::pack_bf16x2(__uint_as_float(pv[2 * c]), __uint_as_float(pv[2 * c + 1]));
+                    ptx::tmem_st16(s_tm, pk);
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before_sync();
+                }
+                __syncwarp();
+                nb_arrive(NB_P_READY + (uint32_t)b, NB_PDS_COUNT);
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4) d4[c4] = __ldg(drow + c4);
+
+                // dP(g).  Its completion also means dK(g-2) and dQ(g-2), the
+                // readers of dS buffer b, are done (they were issued before it).
+                if (ok) ok = warp_wait_bar(bar(L::B_DPFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1400 + L::B_DPFULL);
                 uint32_t dp[32];
-                ptx::tmem_ld32(tmem + lane_off + TM_DP + 32u * half, dp);
-                ptx::tmem_wait_ld(dp);
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_DPREAD));
-                // dS = P (dP - D), bf16 pairs.
-                uint32_t dk2[16];
+                if (!ok) {
 #pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    const float4 d4 = drow[c4];
-                    const float e0 = pf[4 * c4 + 0] * (__uint_as_float(dp[4 * c4 + 0]) - d4.x);
-                    const float e1 = pf[4 * c4 + 1] * (__uint_as_float(dp[4 * c4 + 1]) - d4.y);
-                    const float e2 = pf[4 * c4 + 2] * (__uint_as_float(dp[4 * c4 + 2]) - d4.z);
-                    const float e3 = pf[4 * c4 + 3] * (__uint_as_float(dp[4 * c4 + 3]) - d4.w);
-                    dk2[2 * c4] = ptx::pack_bf16x2(e0, e1);
-                    dk2[2 * c4 + 1] = ptx::pack_bf16x2(e2, e3);
+                    for (int c = 0; c < 32; ++c) dp[c] = 0u;
+                } else {
+                    ptx::tc_fence_after_sync();
+                    ptx::tmem_ld32(tmem + lane_off + TM_DP + 32u * half, dp);
+                    ptx::tmem_wait_ld(dp);
+                    ptx::tc_fence_before_sync();
                 }
-                // dS^T into buffer b (row r, bytes 64*half .. +63, 128-byte
-                // swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7))
-                // once dK / dQ of step g - 2 have read it.
-                if (g >= 2 && !(ok = warp_wait_bar(bar(L::B_DSFREE + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
-                                                   abort_flag, 0x1400 + L::B_DSFREE + b)))
-                    break;
-                const uint32_t row_addr = sbase + L::OFF_DS + b * L::DS_BYTES + (uint32_t)r * 128u;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t chunk = (uint32_t)(half * 4 + u) ^ (uint32_t)(r & 7);
-                    ptx::st_shared_v4(row_addr + chunk * 16u, dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2], dk2[4 * u + 3]);
-                }
-                ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_DSFULL + b));
+                nb_arrive(NB_DP_READ, NB_PDS_COUNT);
+                if (ok) {
+                    // dS = P (dP - D), bf16 pairs, into dS^T buffer b (row r,
+                    // bytes 64*half .. +63, 128-byte swizzle: 16-byte chunk c of
+                    // row r sits at chunk c ^ (r & 7)).
+                    uint32_t dk2[16];
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float e0 = __uint_as_float(pv[4 * c4 + 0]) * (__uint_as_float(dp[4 * c4 + 0]) - d4[c4].x);
+                        const float e1 = __uint_as_float(pv[4 * c4 + 1]) * (__uint_as_float(dp[4 * c4 + 1]) - d4[c4].y);
+                        const float e2 = __uint_as_float(pv[4 * c4 + 2]) * (__uint_as_float(dp[4 * c4 + 2]) - d4[c4].z);
+                        const float e3 = __uint_as_float(pv[4 * c4 + 3]) * (__uint_as_float(dp[4 * c4 + 3]) - d4[c4].w);
+                        dk2[2 * c4] = ptx::pack_bf16x2(e0, e1);
+                        dk2[2 * c4 + 1] = ptx::pack_bf16x2(e2, e3);
+                    }
+                    const uint32_t row_addr = sbase + L::OFF_DS + b * L::DS_BYTES + (uint32_t)r * 128u;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t chunk = (uint32_t)(half * 4 + u) ^ (uint32_t)(r & 7);
+                        ptx::st_shared_v4(row_addr + chunk * 16u, dk2[4 * u], dk2[4 * u + 1], dk2[4 * u + 2],
+                                          dk2[4 * u + 3]);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                __syncwarp();
+                nb_arrive(NB_DS_READY + (uint32_t)b, NB_PDS_COUNT);
             }
         }
     }
@@ -608,8 +638,8 @@ __global__ void __launch_bounds__(256)
     for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// dQ = bf16(scale * accumulator) for rows < N.  Each thread converts 8
-// consecutive elements.
+// dQ = bf16(scale * accumulator) for rows < N; the accumulator is
+// (B*H, Np, D).  Each thread converts 8 consecutive elements.
 __global__ void __launch_bounds__(256)
     fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Np, int D,
                      int64_t n8, float scale)
