@@ -21,6 +21,10 @@ causal mask.
   sample of rows of the same workload (rank 0 only).
 * --impl reference: the oracle alone (the reference arm: the pages ship no
   runnable code), each step a bounded sample of rows.
+* --pass bwd: the backward instead (fa_bwd: gradients dQ, dK, dV for a given
+  dO, d = 128); a step is one fa_bwd call (three launches: prepare, main,
+  dQ conversion) and the FLOPs are those of its five matrix products,
+  10·B·H·N²·d, halved under the causal mask.
 
 With N > 1 (torchrun) every rank runs its own copy of the workload on its own
 GPU: the (batch, head) problems are independent, so there is no data-path
@@ -43,19 +47,28 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak, causal & non-causal"
+BWD_METRIC = "attention bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
 DECODE_METRIC = "attention decode (split-KV): KV-cache bytes read per second"
 
-KERNEL_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
+FWD_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
+BWD_SOURCES = ('fa_bwd_kernel.cuh', 'fa_fwd_kernel.cuh', 'ptx.cuh', 'fa_api.cu')
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload
-# name and the sha256 of the kernel sources it was taken on; reported as
-# roofline.traffic only while the sources still hash the same.  The capture
-# ran B = 2 of the same workload (a smaller launch that still exceeds L2) and
-# is scaled by 4 to a full launch: every (batch, head) problem moves the same
-# bytes.  profiles/ holds the summary and the command.
+# name and pass, with the sha256 of the kernel sources it was taken on;
+# reported as roofline.traffic only while the sources still hash the same.
+# The captures ran B = 2 of the same workload (a smaller launch that still
+# exceeds L2) and are scaled by 4 to a full launch: every (batch, head)
+# problem moves the same bytes.  profiles/ holds the summaries and commands.
 MEASURED_TRAFFIC = {
-    "b8_h32_n4096_d128_causal": {"sha256": "bb5f09a86de176ede95ba6d6d881fd6ca60c5fd29f8847477cc260fe0f631eda",
-                                 "bytes": 4 * (201_426_432 + 45_347_584),
-                                 "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
+    ("b8_h32_n4096_d128_causal", "fwd"): {
+        "sources": FWD_SOURCES,
+        "sha256": "bb5f09a86de176ede95ba6d6d881fd6ca60c5fd29f8847477cc260fe0f631eda",
+        "bytes": 4 * (201_426_432 + 45_347_584),
+        "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
+    ("b8_h32_n4096_d128_causal", "bwd"): {
+        "sources": BWD_SOURCES,
+        "sha256": "a21a7d994a7ac9b538fed68ce5fcb1d207b77bd5e80afc1b9f74176fe2700e75",
+        "bytes": 4 * (405_997_312 + 218_239_232),
+        "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -67,6 +80,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward (default) or the backward")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
@@ -74,19 +89,19 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
-def kernel_sources_sha256() -> str:
+def kernel_sources_sha256(names=FWD_SOURCES) -> str:
     import hashlib
 
     hsh = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         with open(os.path.join(ROOT, "io_aware_attention_gb300", "csrc", name), "rb") as f:
             hsh.update(f.read())
     return hsh.hexdigest()
 
 
-def measured_traffic(workload_name: str):
-    rec = MEASURED_TRAFFIC.get(workload_name)
-    if rec is None or rec["sha256"] != kernel_sources_sha256():
+def measured_traffic(workload_name: str, pass_: str = "fwd"):
+    rec = MEASURED_TRAFFIC.get((workload_name, pass_))
+    if rec is None or rec["sha256"] != kernel_sources_sha256(rec["sources"]):
         return None
     return rec["bytes"]
 
@@ -393,6 +408,170 @@ def run_decode(args, w, rank, world, local):
     return 0
 
 
+def bwd_flops(w) -> float:
+    """FLOPs of one backward: five N x N x d products per (batch, head)
+    (S = QK^T recomputed, dP = dO V^T, dV = P^T dO, dK = dS^T Q, dQ = dS K),
+    2 flops per multiply-add, halved under the causal mask."""
+    f = 10.0 * w.B * w.H * w.N * w.N * w.d
+    return f / 2 if w.causal else f
+
+
+def bwd_oracle_rate(w, q, k, v, do, budget_s: float, max_heads: int = 64):
+    """The fp64 oracle backward on whole heads of the workload (a head is the
+    smallest unit: its gradients need every row), as many as fit the budget.
+    Returns (heads, seconds, TFLOP/s) with the FLOPs of bwd_flops per head."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(11)
+    flat = lambda t: t.reshape(w.B * w.H, 1, 1, w.N, w.d)
+    per_head = 10.0 * w.N * w.N * w.d * (0.5 if w.causal else 1.0)
+    heads, total = 0, 0.0
+    while heads < max_heads and (heads == 0 or total < budget_s):
+        bh = int(rng.integers(0, w.B * w.H))
+        ins = [flat(t)[bh].contiguous() for t in (q, k, v, do)]
+        t0 = time.perf_counter()
+        oracle.attention_bwd(*ins, w.causal, w.scale)
+        total += time.perf_counter() - t0
+        heads += 1
+    return heads, total, heads * per_head / total / 1e12
+
+
+def run_bwd(args, w, config, rank, world, local):
+    """One step = one fa_bwd call (prepare, main kernel, dQ conversion) over the
+    whole workload, with O and the logsumexp from fa_fwd computed once."""
+    import torch
+    import torch.distributed as distm
+
+    import io_aware_attention_gb300 as fa
+    from io_aware_attention_gb300.workloads import make_qkv, make_random_qkv
+
+    flops = bwd_flops(w)
+    config = dict(config, **{"pass": "bwd", "dO": "iid N(0,1) bf16, seeded (seed + 500)"})
+    config["l2"] = (f"inputs {6 * w.B * w.H * w.N * w.d * 2 / 1e6:.0f} MB (q, k, v, o, dO + dq/dk/dv outputs) "
+                    "> 129 MB L2 (no flush)")
+    q_h, k_h, v_h = make_qkv(w)
+    do_h = make_random_qkv(w.B, w.H, w.N, w.d, w.seed + 500)[0]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        warm = max(args.warmup, 3)
+        steps = args.steps
+        bwd_oracle_rate(w, q_h, k_h, v_h, do_h, 0.0, max_heads=1)  # first call: page in, build
+        heads, dt, rate = bwd_oracle_rate(w, q_h, k_h, v_h, do_h, budget_s=60.0, max_heads=max(1, steps))
+        line = {"impl": "reference", "metric": BWD_METRIC, "value": rate, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": heads, "warmup": 1, "ms_per_step": 1e3 * dt / heads, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+                                 "sample": f"{heads} whole random (b,h) heads, one per step (a head is the "
+                                           "oracle backward's smallest unit), fp64, at most 60 s"},
+                "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if w.d != 128:
+        raise SystemExit(f"the backward kernel takes d = 128; workload {w.name} has d = {w.d}")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        distm.init_process_group("nccl", device_id=dev)
+        pg = True
+    q, k, v, do = q_h.to(dev), k_h.to(dev), v_h.to(dev), do_h.to(dev)
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty(fa.bwd_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.bwd_into(q, k, v, o, lse, do, dq, dk, dv, ws, w.causal, w.scale)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if fa.check_device_status() != 0:
+        raise RuntimeError("backward reported a timed-out wait during warm-up")
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg:
+        distm.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        distm.barrier()
+    clocks = sampler.stop() if sampler else None
+    if fa.check_device_status() != 0:
+        raise RuntimeError("backward reported a timed-out wait in the timed region")
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
+    ms_per_step = ms / args.steps
+    value = job_tflops(flops, world, ms_per_step)
+
+    e2e = None
+    if not args.no_e2e:
+        pinned = [t.pin_memory() for t in (q_h, k_h, v_h, do_h)]
+        op, lp = o.cpu().pin_memory(), lse.cpu().pin_memory()
+        outs = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
+
+        def e2e_step():
+            for dst, src in zip((q, k, v, do), pinned):
+                dst.copy_(src, non_blocking=True)
+            o.copy_(op, non_blocking=True)
+            lse.copy_(lp, non_blocking=True)
+            step()
+            for dst, src in zip(outs, (dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+        tb = q.numel() * q.element_size()
+        e2e = {"value": job_tflops(flops, world, ems / n_e2e), "unit": "TFLOP/s", "ms_per_step": ems / n_e2e,
+               "steps": n_e2e, "h2d_bytes_per_step": 5 * tb + lse.numel() * 4, "d2h_bytes_per_step": 3 * tb}
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
+            "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+            "kernel": f"fa::bwd::fa_bwd_kernel<{w.d},{str(w.causal).lower()}>; the timed launch is the whole "
+                      "fa_bwd call (prepare + main + dQ conversion), so this is a lower bound for the main kernel",
+            "traffic": measured_traffic(w.name, "bwd"), "alg_flops_per_launch": flops,
+            "traffic_kernel": "main kernel only (fa_bwd_kernel), DRAM read + write per launch"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        heads, dt, rate = bwd_oracle_rate(w, q_h, k_h, v_h, do_h, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"{heads} whole random (b,h) heads of the workload, fp64 backward, {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": BWD_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * args.steps, "clocks": clocks, "pct_of_peak": round(100 * achieved / peak, 2)}
+        print(json.dumps(line), flush=True)
+    if pg:
+        distm.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
@@ -422,6 +601,8 @@ def main(argv=None):
               "l2": (f"inputs {in_mb:.0f} MB > 129 MB L2 (no flush)" if in_mb > 129 else
                      f"inputs {in_mb:.1f} MB fit in L2 (not flushed: warm-cache figure)")}
 
+    if args.pass_ == "bwd":
+        return run_bwd(args, w, config, rank, world, local)
     if args.impl == "reference":
         return run_reference(args, w, flops, config, rank, world)
 
