@@ -22,7 +22,7 @@ causal mask.
 * --impl reference: the oracle alone (the reference arm: the pages ship no
   runnable code), each step a bounded sample of rows.
 * --pass bwd: the backward instead (fa_bwd: gradients dQ, dK, dV for a given
-  dO, d = 128); a step is one fa_bwd call (three launches: prepare, main,
+  dO, d = 64 or 128); a step is one fa_bwd call (three launches: prepare, main,
   dQ conversion) and the FLOPs are those of its five matrix products,
   10·B·H·N²·d, halved under the causal mask.
 
@@ -472,8 +472,8 @@ def run_bwd(args, w, config, rank, world, local):
         print(json.dumps(line), flush=True)
         return 0
 
-    if w.d != 128:
-        raise SystemExit(f"the backward kernel takes d = 128; workload {w.name} has d = {w.d}")
+    if w.d not in (64, 128):
+        raise SystemExit(f"the backward kernel takes d = 64 or 128; workload {w.name} has d = {w.d}")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pg = None

@@ -157,7 +157,7 @@ fa_status fa_decode_static(const void *q, const void *k, const void *v, void *o,
  * B*H*Np*(d + 2)*4 bytes, Np = N rounded up to a multiple of 64 (the per-row
  * L*log2 e and D, and the fp32 dQ accumulator).  Needs no device.  Errors:
  * FA_ERR_INVALID_ARG (bytes NULL, sizes < 1 or too large),
- * FA_ERR_UNSUPPORTED (d other than 128).  B*H must not exceed 65535.
+ * FA_ERR_UNSUPPORTED (d other than 64 or 128).  B*H must not exceed 65535.
  */
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes);
 
@@ -179,7 +179,7 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, siz
  *              lse fp32 (B, H, N), natural log); same causal and scale.
  *   dout       device pointer, bf16, contiguous (B, H, N, d): dLoss/dO.
  *   dq, dk, dv device pointers, bf16, contiguous (B, H, N, d); fully written.
- *   B, H       B*H <= 65535.  d: 128.  causal: 0 or 1.  scale: finite, > 0
+ *   B, H       B*H <= 65535.  d: 64 or 128.  causal: 0 or 1.  scale: finite, > 0
  *              (the forward's).
  *   workspace, workspace_bytes
  *              device scratch of at least fa_bwd_workspace_bytes(...) bytes,

@@ -12,7 +12,7 @@ logsumexp of each row's scaled, masked scores.
 
     dq, dk, dv = io_aware_attention_gb300.bwd(q, k, v, o, lse, do, causal=True)
 
-gives the gradients for the output gradient ``do`` (d = 128), recomputing the
+gives the gradients for the output gradient ``do`` (d in {64, 128}), recomputing the
 probabilities from ``lse``.
 """
 from __future__ import annotations

@@ -151,7 +151,7 @@ struct BwdShape {
 fa_status bwd_check(int64_t B, int64_t H, int64_t N, int64_t d, BwdShape* sh)
 {
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const int64_t LIM = (int64_t)1 << 60;
     if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
@@ -473,9 +473,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
     // 1. D, L * log2 e, zeroed dQ accumulator.
     const int64_t rows = BH * sh.Np;
-    fa::bwd::fa_bwd_prep_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
-        (int)N, (int)sh.Np, rows);
+    const unsigned prep_grid = (unsigned)((rows + 7) / 8);
+    if (d == 128)
+        fa::bwd::fa_bwd_prep_kernel<128><<<prep_grid, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
+            (int)N, (int)sh.Np, rows);
+    else
+        fa::bwd::fa_bwd_prep_kernel<64><<<prep_grid, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
+            (int)N, (int)sh.Np, rows);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
     // 2. dK, dV and the dQ accumulator.
@@ -493,8 +499,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.scale = scale;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const unsigned grid = (unsigned)std::min<int64_t>((BH * sh.num_kb + 1) / 2, sms);
-    const fa_status ms = causal ? launch_bwd_main<128, true>(mq, mk, mv, mdo, mdq, p, grid, dev, st)
-                                : launch_bwd_main<128, false>(mq, mk, mv, mdo, mdq, p, grid, dev, st);
+    fa_status ms;
+    if (d == 128)
+        ms = causal ? launch_bwd_main<128, true>(mq, mk, mv, mdo, mdq, p, grid, dev, st)
+                    : launch_bwd_main<128, false>(mq, mk, mv, mdo, mdq, p, grid, dev, st);
+    else
+        ms = causal ? launch_bwd_main<64, true>(mq, mk, mv, mdo, mdq, p, grid, dev, st)
+                    : launch_bwd_main<64, false>(mq, mk, mv, mdo, mdq, p, grid, dev, st);
     if (ms != FA_OK) return ms;
 
     // 3. dQ = scale * accumulator, bf16.

@@ -26,12 +26,16 @@
 //   dP^T = V dO^T       (same shape)                              smem x smem
 //   dV  += P^T dO       (M = 128 keys, N = d, K = 64 queries)     TMEM x smem
 //   dK  += dS^T Q       (same shape)                              smem x smem
-//   dQ^T = K^T dS^T     (M = d, N = 64 queries, K = 128 keys)     smem x smem
+//   dQ^T = K^T dS^T     (M = 128, N = 64 queries, K = 128 keys)   smem x smem
 // so a thread of the P/dS warps owns one key row and P^T lands in TMEM in
 // the layout the TS-form dV MMA reads as its A operand.  dS^T is written once
 // to shared memory (128 rows of 128 bytes, 128-byte swizzle); the same bytes
 // are the K-major A operand of the dK MMA and the MN-major B operand of the
 // dQ MMA.  K is the MN-major A operand of the dQ MMA (K^T read in place).
+// That MMA always has M = 128 (the TMEM lanes of a plain M = 128 product):
+// for d = 64 its A operand is K's one 64-column block followed by a block of
+// zeros kept in shared memory, so TMEM lanes 64-127 of dQ^T hold zeros and
+// the dQ warps of those lanes skip the reduce.
 //
 // Warp roles (448 threads):
 //   warps 0-7   P / dS.  Warp w serves keys 32*(w%4) .. +31 (its TMEM lane
@@ -135,15 +139,15 @@ struct Params {
 
 template <int D>
 struct Layout {
-    static_assert(D == 128, "head size");
-    static constexpr uint32_t KV_BYTES = BKV * D * 2;   // K or V of an item (two 64-column blocks)
+    static_assert(D == 64 || D == 128, "head size");
+    static constexpr uint32_t KV_BYTES = BKV * D * 2;   // K or V of an item (D / 64 64-column blocks)
     static constexpr uint32_t KBLK = BKV * 128;         // one 64-column block of K or V (16 KB)
     static constexpr uint32_t QT_BYTES = BQ * D * 2;    // a Q or dO tile
     static constexpr uint32_t QBLK = BQ * 128;          // one 64-column block of it (8 KB)
     static constexpr uint32_t DS_BYTES = BKV * BQ * 2;  // dS^T tile (128 rows x 128 B)
     static constexpr uint32_t STG_WARP = BQ * 32 * 4;   // one dQ warp's fp32 staging (64 x 32)
-    static constexpr uint32_t OFF_K = 0;
-    static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+    static constexpr uint32_t OFF_K = 0;                // two blocks: K, or K and zeros when D = 64
+    static constexpr uint32_t OFF_V = OFF_K + 2 * KBLK;
     static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;
     static constexpr uint32_t OFF_DO = OFF_Q + QSTAGES * QT_BYTES;
     static constexpr uint32_t OFF_DS = OFF_DO + QSTAGES * QT_BYTES;
@@ -242,6 +246,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tmem_alloc(sbase + L::OFF_MISC, TM_COLS);
         ptx::tmem_relinquish();
     }
+    if constexpr (D == 64) {
+        // The zero block after K: head dims 64-127 of the dQ MMA's A operand.
+        for (uint32_t i = threadIdx.x; i < L::KBLK / 16; i += NUM_THREADS)
+            ptx::st_shared_v4(sbase + L::OFF_K + L::KBLK + 16u * i, 0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
+    }
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ----------------------------------------------------- MMA issuer
         constexpr uint32_t ID_S = ptx::idesc_bf16_f32_ab(BKV, BQ, false, false);  // S^T, dP^T
         constexpr uint32_t ID_G = ptx::idesc_bf16_f32_ab(BKV, D, false, true);    // dV, dK
-        constexpr uint32_t ID_Q = ptx::idesc_bf16_f32_ab(D, BQ, true, true);      // dQ^T
+        constexpr uint32_t ID_Q = ptx::idesc_bf16_f32_ab(BKV, BQ, true, true);    // dQ^T (M = 128)
         // K-major descriptors (rows of 128 B, 8-row groups 1024 B apart).
         const uint64_t k_kmaj = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
         const uint64_t v_kmaj = ptx::sdesc_sw128(sbase + L::OFF_V, 16, 1024);
@@ -407,13 +417,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;  // dQ^T lanes = head dims 32*quarter ..; dK/dV lanes = keys
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t stg = sbase + L::OFF_STG + quarter * L::STG_WARP;
+        const bool has_dims = quarter * 32 < D;  // this lane quarter of dQ^T holds head dims
         int g = 0, k = 0;
         bool ok = true;
         for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const Item it = item_of<CAUSAL>(i, p);
             for (int t = 0; t < it.nq; ++t, ++g) {
                 if (ok) ok = warp_wait_bar(bar(L::B_DQFULL), (uint32_t)g & 1u, limit, abort_flag, 0x1300 + L::B_DQFULL);
-                if (ok) {
+                // Every dQ warp waits for dQ(g) before it signals, so that no
+                // warp runs a step ahead on the named barrier.
+                if (ok && has_dims) {
                     uint32_t a[32], c[32];
                     ptx::tc_fence_after_sync();
                     ptx::tmem_ld32(tmem + lane_off + TM_DQ, a);

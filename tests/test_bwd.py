@@ -112,6 +112,36 @@ def test_bwd_parity(B, H, N, causal):
     check_heads(q, k, v, do, causal, scale, dq, dk, dv, range(B * H), f"N={N} causal={causal}")
 
 
+SHAPES_D64 = [  # (B, H, N, causal), head size 64
+    (1, 2, 256, False), (1, 2, 256, True), (1, 1, 1, True), (1, 2, 65, False), (2, 2, 333, True),
+    (1, 1, 1000, False),
+]
+
+
+@pytest.mark.parametrize("B,H,N,causal", SHAPES_D64, ids=[f"d64b{b}h{h}n{n}{'c' if c else ''}" for b, h, n, c in SHAPES_D64])
+def test_bwd_parity_d64(B, H, N, causal):
+    q, k, v = (t.cuda() for t in make_random_qkv(B, H, N, 64, 9800 + N + B))
+    do = make_random_qkv(B, H, N, 64, 9850 + N + B)[0].cuda()
+    scale = 64 ** -0.5
+    dq, dk, dv = run_bwd(q, k, v, do, causal, scale)
+    check_heads(q, k, v, do, causal, scale, dq, dk, dv, range(B * H), f"d=64 N={N} causal={causal}")
+
+
+def test_bwd_d64_stress_workload_sampled_heads():
+    """The d = 64 rescale-stress workload (B16 H16 N8192, Q x4, every 512th
+    key x8, non-causal): whole sampled heads against the oracle."""
+    from io_aware_attention_gb300.workloads import WORKLOADS, make_qkv
+
+    w = WORKLOADS["b16_h16_n8192_d64_spiky"]
+    q, k, v = (t.cuda() for t in make_qkv(w))
+    do = make_random_qkv(w.B, w.H, w.N, w.d, w.seed + 500)[0].cuda()
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa.check_device_status() == 0
+    check_heads(q, k, v, do, w.causal, w.scale, dq, dk, dv, [w.B * w.H - 1], "d=64 stress")
+
+
 def test_bwd_spiky_scores():
     """Large scores (Q = 4 N(0,1)) and every 16th key scaled by 8, so rows are
     dominated by a few keys and P spans many binades."""
