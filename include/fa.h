@@ -37,7 +37,7 @@ typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, non-finite or non-positive
                                 scale, causal not 0/1, o overlapping q/k/v/lse */
-    FA_ERR_UNSUPPORTED = 2,  /* head size not 64/128, pointer not 16-byte aligned
+    FA_ERR_UNSUPPORTED = 2,  /* head size not supported, pointer not 16-byte aligned
                                 (lse: 4-byte), device not sm_103 */
     FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or the launch failed */
     FA_ERR_TIMEOUT = 4,      /* a kernel gave up a pipeline wait (device status) */
@@ -59,7 +59,10 @@ typedef enum fa_status {
  *            natural-log logsumexp of the scaled, masked scores of each row.
  *   B, H, N  batch, heads, sequence length (queries = keys = N); each >= 1,
  *            B*H*N*d < 2^62, B*H*ceil(N/128) < 2^31.
- *   d        head size; 64 or 128.
+ *   d        head size: a multiple of 8 from 8 to 128.  64 and 128 run
+ *            natively; other sizes run in the 64- or 128-column kernel with
+ *            the columns past d read as zeros by the TMA loads (they add
+ *            nothing to any dot product), and only d columns of O are written.
  *   causal   0: every query sees every key; 1: query i sees keys 0..i.
  *   scale    finite, > 0 (typically 1/sqrt(d)); scores are scale * q.k.
  *   stream   CUDA stream the work is enqueued on.
@@ -154,10 +157,12 @@ fa_status fa_decode_static(const void *q, const void *k, const void *v, void *o,
 
 /*
  * fa_bwd_workspace_bytes — device scratch that fa_bwd needs for these sizes:
- * B*H*Np*(d + 2)*4 bytes, Np = N rounded up to a multiple of 64 (the per-row
- * L*log2 e and D, and the fp32 dQ accumulator).  Needs no device.  Errors:
- * FA_ERR_INVALID_ARG (bytes NULL, sizes < 1 or too large),
- * FA_ERR_UNSUPPORTED (d other than 64 or 128).  B*H must not exceed 65535.
+ * B*H*Np*(Dp + 2)*4 bytes, Np = N rounded up to a multiple of 64 and Dp the
+ * padded head size (64 for d <= 64, else 128): the per-row L*log2 e and D,
+ * and the fp32 dQ accumulator, kept at the padded head size.  Needs no
+ * device.  Errors: FA_ERR_INVALID_ARG (bytes NULL, sizes < 1 or too large),
+ * FA_ERR_UNSUPPORTED (d not a multiple of 8 in 8..128).  B*H must not exceed
+ * 65535.
  */
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t *bytes);
 
@@ -179,7 +184,8 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, siz
  *              lse fp32 (B, H, N), natural log); same causal and scale.
  *   dout       device pointer, bf16, contiguous (B, H, N, d): dLoss/dO.
  *   dq, dk, dv device pointers, bf16, contiguous (B, H, N, d); fully written.
- *   B, H       B*H <= 65535.  d: 64 or 128.  causal: 0 or 1.  scale: finite, > 0
+ *   B, H       B*H <= 65535.  d: a multiple of 8 from 8 to 128 (as fa_fwd).
+ *              causal: 0 or 1.  scale: finite, > 0
  *              (the forward's).
  *   workspace, workspace_bytes
  *              device scratch of at least fa_bwd_workspace_bytes(...) bytes,

@@ -75,6 +75,12 @@ bool make_acc_map(CUtensorMap* map, void* base, int64_t BH, int64_t Np, int64_t 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Head sizes the forward and backward take: multiples of 8 up to 128.  They
+// run in the kernel instance for 64 (d <= 64) or 128 columns; the TMA loads
+// fill the columns past d with zeros.  Rows stay 16-byte aligned.
+bool head_size_ok(int64_t d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+int64_t padded_head_size(int64_t d) { return d <= 64 ? 64 : 128; }
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -82,25 +88,25 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 }
 
 // Per-device, per-kernel one-time set-up (opt-in shared memory size).
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAD>
 cudaError_t prepare_kernel(int dev)
 {
     static std::atomic<int> done[MAX_DEVICES];
     if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
     if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL>,
+    cudaError_t e = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, PAD>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)fa::Layout<D>::SMEM_BYTES);
     if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
     return e;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PAD = false>
 fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                  const fa::Params& p, unsigned grid, int dev, cudaStream_t stream)
 {
-    if (prepare_kernel<D, CAUSAL>(dev) != cudaSuccess) return FA_ERR_CUDA;
-    fa::fa_fwd_kernel<D, CAUSAL>
+    if (prepare_kernel<D, CAUSAL, PAD>(dev) != cudaSuccess) return FA_ERR_CUDA;
+    fa::fa_fwd_kernel<D, CAUSAL, PAD>
         <<<grid, fa::NUM_THREADS, fa::Layout<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -144,26 +150,28 @@ cudaError_t prepare_bwd_kernel(int dev)
 }
 
 struct BwdShape {
-    int64_t BH, Np, num_kb;
+    int64_t BH, Np, num_kb, Dp;  // Dp: the kernel instance's (padded) head size
     size_t ws_bytes;
 };
 
 fa_status bwd_check(int64_t B, int64_t H, int64_t N, int64_t d, BwdShape* sh)
 {
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d)) return FA_ERR_UNSUPPORTED;
+    const int64_t Dp = padded_head_size(d);
     const int64_t LIM = (int64_t)1 << 60;
-    if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
+    if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / (Dp + 2)) return FA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
     const int64_t Np = (N + fa::bwd::BQ - 1) / fa::bwd::BQ * fa::bwd::BQ;
     const int64_t num_kb = (N + fa::bwd::BKV - 1) / fa::bwd::BKV;
     // BH is the dQ conversion's grid.y; items are int
     if (Np > INT32_MAX / 2 || BH > 65535 || BH > (int64_t)(INT32_MAX / 2) / num_kb) return FA_ERR_INVALID_ARG;
-    if (BH * Np > LIM / (d + 2)) return FA_ERR_INVALID_ARG;
+    if (BH * Np > LIM / (Dp + 2)) return FA_ERR_INVALID_ARG;
     sh->BH = BH;
     sh->Np = Np;
     sh->num_kb = num_kb;
-    sh->ws_bytes = (size_t)(BH * Np) * (size_t)(d + 2) * sizeof(float);
+    sh->Dp = Dp;
+    sh->ws_bytes = (size_t)(BH * Np) * (size_t)(Dp + 2) * sizeof(float);
     return FA_OK;
 }
 
@@ -367,7 +375,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d)) return FA_ERR_UNSUPPORTED;
     const int64_t LIM = (int64_t)1 << 62;
     if (B > LIM / H || B * H > LIM / N || B * H * N > LIM / d) return FA_ERR_INVALID_ARG;
     const int64_t BH = B * H;
@@ -398,6 +406,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.o = static_cast<__nv_bfloat16*>(o);
     p.lse = lse;
     p.N = (int)N;
+    p.d = (int)d;
     p.num_m_blocks = (int)m_blocks;
     p.num_items = (int)(BH * m_blocks);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
@@ -410,8 +419,14 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (d == 128)
         return causal ? launch<128, true>(mq, mk, mv, p, grid, dev, st)
                       : launch<128, false>(mq, mk, mv, p, grid, dev, st);
-    return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st)
-                  : launch<64, false>(mq, mk, mv, p, grid, dev, st);
+    if (d == 64)
+        return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st)
+                      : launch<64, false>(mq, mk, mv, p, grid, dev, st);
+    if (d > 64)
+        return causal ? launch<128, true, true>(mq, mk, mv, p, grid, dev, st)
+                      : launch<128, false, true>(mq, mk, mv, p, grid, dev, st);
+    return causal ? launch<64, true, true>(mq, mk, mv, p, grid, dev, st)
+                  : launch<64, false, true>(mq, mk, mv, p, grid, dev, st);
 }
 
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t* bytes)
@@ -467,21 +482,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     CUtensorMap mq, mk, mv, mdo, mdq;
     if (!make_map(&mq, q, BH, N, d, fa::bwd::BQ) || !make_map(&mk, k, BH, N, d, fa::bwd::BKV) ||
         !make_map(&mv, v, BH, N, d, fa::bwd::BKV) || !make_map(&mdo, dout, BH, N, d, fa::bwd::BQ) ||
-        !make_acc_map(&mdq, acc, BH, sh.Np, d))
+        !make_acc_map(&mdq, acc, BH, sh.Np, sh.Dp))
         return FA_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     // 1. D, L * log2 e, zeroed dQ accumulator.
     const int64_t rows = BH * sh.Np;
-    const unsigned prep_grid = (unsigned)((rows + 7) / 8);
-    if (d == 128)
-        fa::bwd::fa_bwd_prep_kernel<128><<<prep_grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
-            (int)N, (int)sh.Np, rows);
-    else
-        fa::bwd::fa_bwd_prep_kernel<64><<<prep_grid, 256, 0, st>>>(
-            static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
-            (int)N, (int)sh.Np, rows);
+    fa::bwd::fa_bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
+        (int)N, (int)sh.Np, (int)d, (int)sh.Dp, rows);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
 
     // 2. dK, dV and the dQ accumulator.
@@ -492,6 +501,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.dsum = dsum;
     p.dq_acc = acc;
     p.N = (int)N;
+    p.d = (int)d;
     p.Np = (int)sh.Np;
     p.num_kb = (int)sh.num_kb;
     p.num_items = (int)(BH * sh.num_kb);
@@ -500,7 +510,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const unsigned grid = (unsigned)std::min<int64_t>((BH * sh.num_kb + 1) / 2, sms);
     fa_status ms;
-    if (d == 128)
+    if (sh.Dp == 128)
         ms = causal ? launch_bwd_main<128, true>(mq, mk, mv, mdo, mdq, p, grid, dev, st)
                     : launch_bwd_main<128, false>(mq, mk, mv, mdo, mdq, p, grid, dev, st);
     else
@@ -511,7 +521,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     // 3. dQ = scale * accumulator, bf16.
     const int64_t n8 = BH * N * d / 8;
     fa::bwd::fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
-        acc, static_cast<__nv_bfloat16*>(dq), (int)N, (int)sh.Np, (int)d, n8, scale);
+        acc, static_cast<__nv_bfloat16*>(dq), (int)N, (int)sh.Np, (int)d, (int)sh.Dp, n8, scale);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -127,8 +127,9 @@ struct Params {
     __nv_bfloat16* dv;
     const float* lse2;  // (B*H, Np): L * log2 e; +inf for rows >= N
     const float* dsum;  // (B*H, Np): D; 0 for rows >= N
-    float* dq_acc;      // (B*H, Np, d): fp32 dQ / scale
+    float* dq_acc;      // (B*H, Np, D): fp32 dQ / scale (D = the padded head size)
     int N;
+    int d;         // the caller's head size (<= D, a multiple of 8): dK, dV row stride and stored columns
     int Np;        // query rows rounded up to a multiple of BQ
     int num_kb;    // key blocks per head
     int num_items; // B*H*num_kb
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int quarter = warp & 3;  // dQ^T lanes = head dims 32*quarter ..; dK/dV lanes = keys
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t stg = sbase + L::OFF_STG + quarter * L::STG_WARP;
-        const bool has_dims = quarter * 32 < D;  // this lane quarter of dQ^T holds head dims
+        const bool has_dims = quarter * 32 < p.d;  // this lane quarter of dQ^T holds head dims
         int g = 0, k = 0;
         bool ok = true;
         for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
@@ -465,7 +466,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const bool key_ok = key < N;
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
-                    __nv_bfloat16* const dst = (which ? p.dk : p.dv) + ((int64_t)it.bh * N + key) * D;
+                    __nv_bfloat16* const dst = (which ? p.dk : p.dv) + ((int64_t)it.bh * N + key) * p.d;
                     const float mul = which ? p.scale : 1.0f;
 #pragma unroll
                     for (int ch = 0; ch < D / 32; ++ch) {
@@ -479,8 +480,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (key_ok) {
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
-                                ptx::st_global_v4(dst + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                  w[4 * u + 3]);
+                                if (ch * 32 + u * 8 < p.d)
+                                    ptx::st_global_v4(dst + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                      w[4 * u + 3]);
                         }
                     }
                 }
@@ -609,36 +611,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // D_i = dO_i . O_i and L_i * log2 e for every row i < Np of every head (rows
 // >= N: D = 0, L * log2 e = +inf, so their recomputed P is 0), and the fp32
-// dQ accumulator zeroed.  One warp per row.
-template <int D>
+// dQ accumulator (Dp floats a row) zeroed.  One warp per row; a lane takes 8
+// consecutive elements (d is a multiple of 8, at most 256 per pass).
 __global__ void __launch_bounds__(256)
     fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dsum,
-                       float* __restrict__ dq_acc, int N, int Np, int64_t rows)
+                       float* __restrict__ dq_acc, int N, int Np, int d, int Dp, int64_t rows)
 {
     const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const int64_t bh = row / Np;
     const int i = (int)(row - bh * Np);
-    constexpr int E = D / 32;  // elements per lane
     float acc = 0.f;
     if (i < N) {
-        const int64_t base = (bh * N + i) * D + lane * E;
-        if constexpr (E == 4) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-            const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
-            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.x));
-            const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a.y));
-            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.x));
-            const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b.y));
-            acc = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
-        } else {
-            const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
-            const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base);
-            const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a));
-            const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b));
-            acc = a0.x * b0.x + a0.y * b0.y;
+        const int64_t base = (bh * N + i) * d;
+        for (int c = lane * 8; c < d; c += 256) {
+            const uint4 a = *reinterpret_cast<const uint4*>(o + base + c);
+            const uint4 b = *reinterpret_cast<const uint4*>(dout + base + c);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[j]));
+                const float2 bf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[j]));
+                acc = fmaf(af.x, bf.x, acc);
+                acc = fmaf(af.y, bf.y, acc);
+            }
         }
     }
 #pragma unroll
@@ -647,24 +645,24 @@ __global__ void __launch_bounds__(256)
         dsum[row] = i < N ? acc : 0.f;
         lse2[row] = i < N ? lse[bh * N + i] * 1.4426950408889634074f : __int_as_float(0x7f800000);
     }
-    float4* const z = reinterpret_cast<float4*>(dq_acc + row * D);
-    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* const z = reinterpret_cast<float4*>(dq_acc + row * Dp);
+    for (int c = lane; c < Dp / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = bf16(scale * accumulator) for rows < N; the accumulator is
-// (B*H, Np, D).  Each thread converts 8 consecutive elements.
+// (B*H, Np, Dp), dQ (B*H, N, d).  Each thread converts 8 consecutive elements.
 __global__ void __launch_bounds__(256)
-    fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Np, int D,
-                     int64_t n8, float scale)
+    fa_bwd_dq_kernel(const float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dq, int N, int Np, int d,
+                     int Dp, int64_t n8, float scale)
 {
     const int64_t e8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e8 >= n8) return;
     const int64_t e = e8 * 8;
-    const int64_t row = e / D;  // bh * N + i
-    const int col = (int)(e - row * D);
+    const int64_t row = e / d;  // bh * N + i
+    const int col = (int)(e - row * d);
     const int64_t bh = row / N;
     const int64_t i = row - bh * N;
-    const float4* const src = reinterpret_cast<const float4*>(dq_acc + (bh * Np + i) * D + col);
+    const float4* const src = reinterpret_cast<const float4*>(dq_acc + (bh * Np + i) * Dp + col);
     const float4 a = src[0], b = src[1];
     uint4 w;
     w.x = ptx::pack_bf16x2(a.x * scale, a.y * scale);

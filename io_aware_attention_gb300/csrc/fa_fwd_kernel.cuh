@@ -58,6 +58,10 @@
 // max by more than RESCALE_LOG2 (base-2 units); P, l and l~ share the same
 // reference, so the ratios are unaffected and P stays below 2^RESCALE_LOG2.
 //
+// Head sizes d < D (multiples of 8) run in the D = 64 or 128 instance: the
+// TMA boxes are 64 columns wide and fill columns past d with zeros, which add
+// nothing to any dot product; the epilogue stores d columns with row stride d.
+//
 // Every wait is bounded in time; on expiry the thread records the wait in the
 // device status word, raises a CTA-wide abort flag, and all roles drain their
 // in-flight copies / MMAs and reach the common exit, where TMEM is freed.
@@ -96,6 +100,7 @@ struct Params {
     __nv_bfloat16* o;
     float* lse;
     int N;
+    int d;  // the caller's head size (<= D, a multiple of 8): O's row stride and stored columns
     int num_m_blocks;
     int num_items;
     float scale_log2;  // scale * log2(e)
@@ -275,7 +280,9 @@ __device__ __forceinline__ Item item_of(int i, const Params& p)
     return it;
 }
 
-template <int D, bool CAUSAL>
+// PAD: the caller's head size p.d is below D (stores are guarded and strided
+// by p.d); the instances for d = D compile without the guard.
+template <int D, bool CAUSAL, bool PAD>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -709,7 +716,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float l = __uint_as_float(la) + __uint_as_float(lb);
                 const float inv_l = 1.0f / __uint_as_float(lt[0]);
                 const bool row_ok = q_idx < N;
-                __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * D + half * (D / 2);
+                // A head size d below D was zero-padded by the TMA loads: the
+                // padded columns of O are zero and not stored.
+                __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
 #pragma unroll
                 for (int ch = 0; ch < D / 64; ++ch) {
                     uint32_t o[32];
@@ -723,8 +732,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (row_ok) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                              w[4 * u + 3]);
+                            if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
+                                ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                  w[4 * u + 3]);
                     }
                 }
                 if (half == 0 && row_ok)

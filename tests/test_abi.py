@@ -59,7 +59,7 @@ def call(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, N=16, d=64, c
     (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1), (dict(d=0), 1),
     (dict(causal=2), 1), (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(scale=0.0), 1), (dict(scale=-0.1), 1),
-    (dict(d=96), 2), (dict(d=256), 2),
+    (dict(d=100), 2), (dict(d=136), 2), (dict(d=4), 2), (dict(d=256), 2),  # head size: multiples of 8 to 128
     (dict(q=P + 8), 2), (dict(o=4 * P + 4), 2), (dict(lse=5 * P + 2), 2),
     (dict(o=P), 1),                       # o aliases q
     (dict(o=3 * P + 16), 1),              # o overlaps the tail of v
@@ -127,7 +127,7 @@ def call_bwd(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, do=6 * P, dq=7 * P,
     (dict(q=0), 1), (dict(o=0), 1), (dict(lse=0), 1), (dict(do=0), 1), (dict(dq=0), 1), (dict(dv=0), 1),
     (dict(ws=0), 1), (dict(B=0), 1), (dict(N=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
     (dict(scale=float("nan")), 1),
-    (dict(d=96), 2), (dict(d=256), 2),                # head size
+    (dict(d=100), 2), (dict(d=256), 2), (dict(d=4), 2),  # head size
     (dict(do=6 * P + 8), 2), (dict(dk=8 * P + 2), 2), (dict(lse=5 * P + 2), 2), (dict(ws=10 * P + 4), 2),
     (dict(ws_bytes=64 * 130 * 4 - 16), 1),            # workspace one row short
     (dict(dq=P), 1),                                  # dq aliases q
@@ -150,6 +150,10 @@ def test_bwd_workspace_bytes(lib):
     assert out.value == 64 * 130 * 4
     assert lib.fa_bwd_workspace_bytes(1, 1, 64, 64, ctypes.byref(out)) == 0
     assert out.value == 64 * 66 * 4
-    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 96, ctypes.byref(out)) == 2
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 96, ctypes.byref(out)) == 0  # padded to 128 columns
+    assert out.value == 64 * 130 * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 40, ctypes.byref(out)) == 0  # padded to 64
+    assert out.value == 64 * 66 * 4
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64, 100, ctypes.byref(out)) == 2
     assert lib.fa_bwd_workspace_bytes(1, 1, 0, 128, ctypes.byref(out)) == 1
     assert lib.fa_bwd_workspace_bytes(1, 1, 64, 128, None) == 1

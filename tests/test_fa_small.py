@@ -105,5 +105,6 @@ def test_python_checks_reject_bad_tensors():
     with pytest.raises(ValueError):
         fa.fwd(q.transpose(2, 3), k, v)
     with pytest.raises(fa.FaError) as e:
-        fa.fwd(q[..., :32].contiguous(), k[..., :32].contiguous(), v[..., :32].contiguous())
+        # head sizes must be multiples of 8 (up to 128)
+        fa.fwd(q[..., :36].contiguous(), k[..., :36].contiguous(), v[..., :36].contiguous())
     assert e.value.code == 2
