@@ -21,6 +21,10 @@ and "Writing and Benchmarking Custom Kernels" §10.3.1):
 D_i) for a given dO, by the softmax/matrix-product chain rule that
 "Writing and Benchmarking Custom Kernels" §10.3.2 describes.
 
+``bias_gelu_dropout`` is the elementwise chain of "Fusion and IO-aware
+kernels" (bias add, GELU in the tanh form of "Writing and Benchmarking
+Custom Kernels" §10.2.1, dropout with a passed-in keep mask), in fp64.
+
 Inputs are torch bf16 CPU tensors (or numpy uint16 arrays of bf16 bits) of
 shape (B, H, N, d), contiguous.  Outputs are numpy float64.
 """
@@ -93,9 +97,11 @@ class Oracle:
         lib.oracle_attn_rect_rows_f64.argtypes = rect + [i64p, i64p, i64, f64p, f64p, c_int]
         lib.oracle_attn_bwd_f64.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, i64, c_int,
                                             c_dbl, f64p, f64p, f64p, f64p, c_int]
+        lib.oracle_bias_gelu_dropout_f64.argtypes = [u16p, u16p, ctypes.POINTER(ctypes.c_uint32), i64, i64,
+                                                     c_dbl, f64p, c_int]
         for fn in (lib.oracle_attn_f64, lib.oracle_attn_rows_f64, lib.oracle_attn_online_f64,
                    lib.oracle_max_threads, lib.oracle_attn_rect_f64, lib.oracle_attn_rect_rows_f64,
-                   lib.oracle_attn_bwd_f64):
+                   lib.oracle_attn_bwd_f64, lib.oracle_bias_gelu_dropout_f64):
             fn.restype = c_int
         self.lib = lib
 
@@ -235,6 +241,27 @@ class Oracle:
             raise RuntimeError(f"oracle_attn_bwd_f64 failed ({rc})")
         return dq, dk, dv, dsum
 
+    def bias_gelu_dropout(self, x, bias, keep, p: float, threads: int = 0):
+        """y = dropout(gelu(x + bias)) in fp64 for x (rows, cols) and bias (cols,),
+        bf16; keep: uint32 words of keep bits over the flat index (bit e % 32 of
+        word e // 32), or None to keep every element.  Returns (rows, cols) float64."""
+        xb, bb = _bits(x), _bits(bias)
+        if xb.ndim != 2 or bb.shape != (xb.shape[1],):
+            raise ValueError(f"x (rows, cols) and bias (cols,) expected: {xb.shape} {bb.shape}")
+        rows, cols = (int(s) for s in xb.shape)
+        kw = None
+        if keep is not None:
+            kw = np.ascontiguousarray(np.asarray(keep, dtype=np.uint32))
+            if kw.size * 32 < rows * cols:
+                raise ValueError("keep mask too short")
+        y = np.empty((rows, cols), np.float64)
+        rc = self.lib.oracle_bias_gelu_dropout_f64(_ptr(xb, ctypes.c_uint16), _ptr(bb, ctypes.c_uint16),
+                                                   _ptr(kw, ctypes.c_uint32), rows, cols, float(p),
+                                                   _ptr(y, ctypes.c_double), int(threads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_bias_gelu_dropout_f64 failed ({rc})")
+        return y
+
 
 def _shape_rect(q, k, v):
     if q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
@@ -290,3 +317,7 @@ def attention_rect_rows(q, k, v, causal, scale, bh_idx, row_idx, threads=0):
 
 def attention_bwd(q, k, v, do, causal, scale, threads=0):
     return _oracle().attention_bwd(q, k, v, do, causal, scale, threads)
+
+
+def bias_gelu_dropout(x, bias, keep, p, threads=0):
+    return _oracle().bias_gelu_dropout(x, bias, keep, p, threads)

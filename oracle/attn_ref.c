@@ -464,3 +464,37 @@ int oracle_attn_bwd_f64(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     free(dOw);
     return failed ? -2 : 0;
 }
+
+/* ------------------------------------------------------------------------
+ * Fused elementwise chain: bias add, GELU, dropout.
+ *
+ * Sources: "Fusion and IO-aware kernels" § The idea in one minute (a bias
+ * add, a GELU and a dropout, each an HBM round trip when run separately) and
+ * its fusion.py byte count; "Writing and Benchmarking Custom Kernels"
+ * §10.2.1 (the tanh form of GELU the chapter's kernel computes).  For element
+ * (r, c) of a rows x cols tensor, flat index e = r*cols + c:
+ *
+ *     h = x[r][c] + bias[c]
+ *     g = 0.5 h (1 + tanh( sqrt(2/pi) (h + 0.044715 h^3) ))
+ *     y = g / (1 - p)   if bit (e % 32) of keep[e / 32] is set, else 0
+ *
+ * The dropout draws are passed in as the packed keep mask (NULL: keep all).
+ * x, bias: bf16 bits; y: rows*cols doubles.  Returns 0, -1 on bad arguments.
+ * ------------------------------------------------------------------------ */
+int oracle_bias_gelu_dropout_f64(const uint16_t *x, const uint16_t *bias, const uint32_t *keep,
+                                 int64_t rows, int64_t cols, double p, double *y, int nthreads)
+{
+    if (!x || !bias || !y || rows < 1 || cols < 1 || !(p >= 0.0 && p < 1.0)) return -1;
+    const double k0 = sqrt(2.0 / 3.14159265358979323846);
+#pragma omp parallel for schedule(static) num_threads(pick_threads(nthreads))
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            const int64_t e = r * cols + c;
+            const double h = bf16_bits_to_f64(x[e]) + bf16_bits_to_f64(bias[c]);
+            const double g = 0.5 * h * (1.0 + tanh(k0 * (h + 0.044715 * h * h * h)));
+            const int kept = keep ? (int)((keep[e >> 5] >> (e & 31)) & 1u) : 1;
+            y[e] = kept ? g / (1.0 - p) : 0.0;
+        }
+    }
+    return 0;
+}

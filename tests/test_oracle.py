@@ -31,6 +31,18 @@ Custom Kernels" §10.3.2) is pinned by:
     equals dO_i . O_i (the page's form of the row scalar); a single key gives
     dV = dO and dQ = dK = 0; under the causal mask keys after the last row
     with a nonzero dO get no gradient; key permutation permutes dK, dV.
+
+The fused elementwise chain (bias + GELU + dropout; "Fusion and IO-aware
+kernels", "Writing and Benchmarking Custom Kernels" §10.2.1) is pinned by:
+  * the exact GELU x·Phi(x) (scipy's normal cdf) within 4.8e-4 over
+    [-8, 8]: the tanh form's own maximum departure is 4.73e-4;
+  * the exact identity g(-h) = g(h) - h (tanh is odd), g(0) = 0, g(h) = h and
+    g(-h) = 0 far out, and (g(h) - h/2) / h^2 -> 1/sqrt(2 pi) as h -> 0;
+  * bias broadcast: on integer data (exact in bf16) x + bias through the
+    oracle equals the sum fed in with a zero bias, with rows != cols;
+  * dropout: kept elements are the undropped values divided by (1 - p),
+    dropped ones exactly 0, and the mask bit of element e is bit e % 32 of
+    word e // 32.
 """
 import math
 import os
@@ -388,12 +400,68 @@ def pin_bwd_key_permutation(orc):
     np.testing.assert_allclose(dv2, dv[:, :, perm.numpy()], rtol=1e-12, atol=1e-13)
 
 
+def _ew_inputs(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    return bf16(rng.standard_normal((rows, cols)) * 2.0), bf16(rng.standard_normal(cols))
+
+
+def pin_gelu_exact_library(orc):
+    """The tanh form stays within its known 4.73e-4 of x*Phi(x) (scipy.special.ndtr)."""
+    x = bf16(np.linspace(-8, 8, 4097).reshape(1, -1))
+    y = orc.bias_gelu_dropout(x, bf16(np.zeros(4097)), None, 0.0)
+    X = f64(x)
+    assert np.abs(y - X * scipy.special.ndtr(X)).max() <= 4.8e-4
+
+
+def pin_gelu_identities(orc):
+    """g(-h) = g(h) - h; g(0) = 0; g far out; the h^2 coefficient at 0."""
+    x = bf16(np.linspace(-5, 5, 513).reshape(1, -1))
+    zero = bf16(np.zeros(513))
+    g = orc.bias_gelu_dropout(x, zero, None, 0.0)
+    gn = orc.bias_gelu_dropout(bf16(-f64(x)), zero, None, 0.0)
+    np.testing.assert_allclose(gn, g - f64(x), rtol=0, atol=1e-14)
+    t = bf16(np.array([[0.0, 9.0, -9.0, 2.0 ** -12]]))
+    y = orc.bias_gelu_dropout(t, bf16(np.zeros(4)), None, 0.0)[0]
+    assert y[0] == 0.0 and abs(y[1] - 9.0) < 1e-14 and abs(y[2]) < 1e-14
+    h = 2.0 ** -12
+    assert abs((y[3] - h / 2) / h ** 2 - 1 / math.sqrt(2 * math.pi)) < 1e-3
+
+
+def pin_bias_broadcast(orc):
+    """Integer data (exact in bf16): gelu(x + bias) with bias per column equals
+    gelu of the materialised sum with a zero bias."""
+    rng = np.random.default_rng(61)
+    xi = rng.integers(-4, 5, size=(5, 7)).astype(np.float64)
+    bi = rng.integers(-3, 4, size=(7,)).astype(np.float64)
+    y1 = orc.bias_gelu_dropout(bf16(xi), bf16(bi), None, 0.0)
+    y2 = orc.bias_gelu_dropout(bf16(xi + bi), bf16(np.zeros(7)), None, 0.0)
+    np.testing.assert_array_equal(y1, y2)
+
+
+def pin_dropout_mask(orc):
+    """Kept: undropped / (1 - p); dropped: exactly 0; bit e % 32 of word e // 32."""
+    x, b = _ew_inputs(6, 40, 62)
+    n = 6 * 40
+    words = np.random.default_rng(63).integers(0, 2 ** 32, size=(n + 31) // 32 + 32, dtype=np.uint64).astype(np.uint32)
+    p = 0.25
+    full = orc.bias_gelu_dropout(x, b, None, 0.0)
+    y = orc.bias_gelu_dropout(x, b, words, p)
+    bits = np.array([(int(words[e >> 5]) >> (e & 31)) & 1 for e in range(n)], bool).reshape(6, 40)
+    assert (y[~bits] == 0).all()
+    np.testing.assert_allclose(y[bits], full[bits] / (1 - p), rtol=1e-15, atol=0)
+    one = np.zeros_like(words)
+    one[37 >> 5] = np.uint32(1 << (37 & 31))
+    y1 = orc.bias_gelu_dropout(x, b, one, 0.5)
+    assert np.count_nonzero(y1) == (1 if full.flat[37] != 0 else 0) and y1.flat[37] == full.flat[37] * 2
+
+
 PINS = [pin_library_softmax, pin_single_key, pin_equal_scores, pin_two_keys,
         pin_probability_rows, pin_constant_values, pin_score_shift, pin_key_permutation,
         pin_causal_prefix, pin_huge_scores, pin_rows_entry, pin_online_recurrence,
         pin_rect_is_square_when_nq_is_nk, pin_rect_bottom_right, pin_rect_single_query_library,
         pin_rect_rows_entry, pin_bwd_autograd, pin_bwd_finite_differences, pin_bwd_invariants,
-        pin_bwd_single_key, pin_bwd_causal_tail, pin_bwd_key_permutation]
+        pin_bwd_single_key, pin_bwd_causal_tail, pin_bwd_key_permutation, pin_gelu_exact_library,
+        pin_gelu_identities, pin_bias_broadcast, pin_dropout_mask]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -447,6 +515,14 @@ MUTANTS = [
      "const int64_t visible = causal ? (i > 0 ? i : 1) : N;"),
     ("backward: dP from the keys", "for (int64_t c = 0; c < d; ++c) g += dOw[i * d + c] * Vw[j * d + c];",
      "for (int64_t c = 0; c < d; ++c) g += dOw[i * d + c] * Kw[j * d + c];"),
+    ("gelu: the one half dropped", "const double g = 0.5 * h * (1.0 + tanh(", "const double g = h * (1.0 + tanh("),
+    ("gelu: tanh sign", "const double g = 0.5 * h * (1.0 + tanh(", "const double g = 0.5 * h * (1.0 - tanh("),
+    ("gelu: cubic term dropped", "(h + 0.044715 * h * h * h)", "(h)"),
+    ("gelu: sqrt(2/pi) dropped", "tanh(k0 * (h + ", "tanh(1.0 * (h + "),
+    ("bias indexed by row", "bf16_bits_to_f64(bias[c])", "bf16_bits_to_f64(bias[r % cols])"),
+    ("mask bit order reversed", "(keep[e >> 5] >> (e & 31))", "(keep[e >> 5] >> (31 - (e & 31)))"),
+    ("dropout scale inverted", "y[e] = kept ? g / (1.0 - p) : 0.0;", "y[e] = kept ? g * (1.0 - p) : 0.0;"),
+    ("dropout keeps dropped values", "y[e] = kept ? g / (1.0 - p) : 0.0;", "y[e] = kept ? g / (1.0 - p) : g;"),
 ]
 
 
