@@ -21,6 +21,9 @@ causal mask.
   sample of rows of the same workload (rank 0 only).
 * --impl reference: the oracle alone (the reference arm: the pages ship no
   runnable code), each step a bounded sample of rows.
+* --workload ew_*: the fused elementwise chain (bias + GELU + dropout) of
+  the pages' fusion discussion; one step is one fa_bias_gelu_dropout launch,
+  the metric its algorithmic bytes per second against the HBM copy peak.
 * --pass bwd: the backward instead (fa_bwd: gradients dQ, dK, dV for a given
   dO, d = 64 or 128); a step is one fa_bwd call (three launches: prepare, main,
   dQ conversion) and the FLOPs are those of its five matrix products,
@@ -49,6 +52,7 @@ if ROOT not in sys.path:
 METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak, causal & non-causal"
 BWD_METRIC = "attention bwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
 DECODE_METRIC = "attention decode (split-KV): KV-cache bytes read per second"
+EW_METRIC = "fused bias+GELU+dropout (bf16): HBM bytes per second (x, bias, keep mask read once, y written once)"
 
 FWD_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
 BWD_SOURCES = ('fa_bwd_kernel.cuh', 'fa_fwd_kernel.cuh', 'ptx.cuh', 'fa_api.cu')
@@ -572,11 +576,162 @@ def run_bwd(args, w, config, rank, world, local):
     return 0
 
 
+def ew_bytes(w) -> int:
+    """Algorithmic bytes of one fused step: x read and y written once (bf16),
+    the packed keep mask and the bias read once."""
+    n = w.rows * w.cols
+    return 4 * n + ((n + 31) // 32) * 4 + 2 * w.cols
+
+
+def ew_oracle_rate(w, x, b, keep, budget_s: float):
+    """The fp64 oracle on the first rows of the workload, as many as fit the
+    budget; algorithmic bytes of those rows per second."""
+    import numpy as np
+
+    import oracle
+
+    words = keep.numpy().view(np.uint32)
+    rows = 64
+    while True:
+        t0 = time.perf_counter()
+        oracle.bias_gelu_dropout(x[:rows], b, words, w.p)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or rows >= w.rows:
+            break
+        rows = min(w.rows, rows * 4)
+    n = rows * w.cols
+    return rows, dt, (4 * n + n / 8 + 2 * w.cols) / dt / 1e9
+
+
+def run_ew(args, w, rank, world, local):
+    """One step = one fa_bias_gelu_dropout launch over the whole tensor."""
+    import torch
+    import torch.distributed as distm
+
+    import io_aware_attention_gb300 as fa
+    from io_aware_attention_gb300.workloads import make_ew_inputs
+
+    nbytes = ew_bytes(w)
+    config = {"workload": w.name, "rows": w.rows, "cols": w.cols, "p": w.p,
+              "inputs": "x ~ N(0,4) bf16, bias ~ N(0,1) bf16, keep bits Bernoulli(1-p), seeded",
+              "per_gpu_problem": True, "parallelism": f"replicas x{args.gpus}",
+              "l2": f"x + y {4 * w.rows * w.cols / 1e6:.0f} MB > 129 MB L2 (no flush)"}
+    x_h, b_h, k_h = make_ew_inputs(w.rows, w.cols, w.p, w.seed)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        import oracle
+        ew_oracle_rate(w, x_h, b_h, k_h, 0.5)
+        tot_b, tot_t, rows = 0.0, 0.0, 0
+        for _ in range(min(args.steps, 20)):
+            rows, dt, rate = ew_oracle_rate(w, x_h, b_h, k_h, 2.0)
+            tot_b += rate * dt * 1e9
+            tot_t += dt
+        value = tot_b / tot_t / 1e9
+        steps = min(args.steps, 20)
+        line = {"impl": "reference", "metric": EW_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": steps, "warmup": 1, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+                                 "sample": f"the first {rows} rows per step, fp64"},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "gpu_launches": 0}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        distm.init_process_group("nccl", device_id=dev)
+        pg = True
+    x, b, keep = x_h.to(dev), b_h.to(dev), k_h.to(dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.bias_gelu_dropout(x, b, keep, w.p, out=y)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg:
+        distm.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        distm.barrier()
+    clocks = sampler.stop() if sampler else None
+    ms_per_step = max_over_ranks(ev0.elapsed_time(ev1), dev) / args.steps
+    value = nbytes * world / (ms_per_step * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        xp, bp, kp = x_h.pin_memory(), b_h.pin_memory(), k_h.pin_memory()
+        yp = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+
+        def e2e_step():
+            x.copy_(xp, non_blocking=True)
+            b.copy_(bp, non_blocking=True)
+            keep.copy_(kp, non_blocking=True)
+            step()
+            yp.copy_(y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), dev) / n_e2e
+        e2e = {"value": nbytes * world / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems, "steps": n_e2e,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (x, b, keep)),
+               "d2h_bytes_per_step": y.numel() * y.element_size()}
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["hbm_gbs"])
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"hbm_gbs (copy), {peak_src}",
+            "kernel": "fa::ew::fa_bias_gelu_dropout_kernel<false>", "traffic": measured_traffic(w.name, "ew"),
+            "alg_bytes_per_launch": nbytes}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rows, dt, rate = ew_oracle_rate(w, x_h, b_h, k_h, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"the first {rows} rows of the workload, fp64, {dt:.1f} s"}
+    if rank == 0:
+        line = {"metric": EW_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": args.steps, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if pg:
+        distm.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
     from io_aware_attention_gb300 import iomodel
-    from io_aware_attention_gb300.workloads import DECODE_WORKLOADS, HEADLINE, WORKLOADS, Workload
+    from io_aware_attention_gb300.workloads import DECODE_WORKLOADS, EW_WORKLOADS, HEADLINE, WORKLOADS, Workload
+
+    if args.workload in EW_WORKLOADS:
+        return run_ew(args, EW_WORKLOADS[args.workload], rank, world, local)
 
     if args.workload in DECODE_WORKLOADS:
         wd = DECODE_WORKLOADS[args.workload]

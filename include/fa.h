@@ -208,6 +208,35 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  fa_stream_t stream);
 
 /*
+ * fa_bias_gelu_dropout — the fused elementwise chain of "Fusion and IO-aware
+ * kernels" (§ The idea in one minute: a bias add, a GELU and a dropout, one
+ * HBM read and one HBM write instead of three round trips), with the tanh
+ * form of GELU of "Writing and Benchmarking Custom Kernels" §10.2.1.  For
+ * element (r, c), flat index e = r*cols + c:
+ *     h = x[r][c] + bias[c]
+ *     g = 0.5 h (1 + tanh(sqrt(2/pi) (h + 0.044715 h^3)))
+ *     y[r][c] = g / (1 - p) if bit e % 32 of keep[e / 32] is set, else 0
+ *
+ * Arguments
+ *   x        device pointer, bf16, contiguous (rows, cols).
+ *   bias     device pointer, bf16, (cols).
+ *   keep     device pointer, uint32 words of keep bits over the flat index
+ *            (ceil(rows*cols / 32) words; the dropout's random draws, made by
+ *            the caller), or NULL to keep every element.
+ *   y        device pointer, bf16, contiguous (rows, cols); fully written.
+ *   rows, cols  >= 1; cols a multiple of 8 (else FA_ERR_UNSUPPORTED).
+ *   p        dropout probability, 0 <= p < 1; kept values are scaled by 1/(1-p).
+ *   stream   CUDA stream the one launch is enqueued on.
+ *
+ * Ownership: the caller owns every buffer.  x, bias, y 16-byte aligned and
+ * keep 4-byte aligned, else FA_ERR_UNSUPPORTED.  y may not overlap x, bias or
+ * keep (FA_ERR_INVALID_ARG); x may be y's input only out of place.
+ * Asynchrony and FA_ERR_CUDA as for fa_fwd.
+ */
+fa_status fa_bias_gelu_dropout(const void *x, const void *bias, const uint32_t *keep, void *y,
+                               int64_t rows, int64_t cols, float p, fa_stream_t stream);
+
+/*
  * fa_check_device_status — synchronises `stream`, reads and clears the
  * device-side status word of the current device.  Returns FA_ERR_TIMEOUT if a
  * kernel launched since the last check gave up a bounded wait (its outputs are

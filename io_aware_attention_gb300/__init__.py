@@ -14,6 +14,11 @@ logsumexp of each row's scaled, masked scores.
 
 gives the gradients for the output gradient ``do`` (d in {64, 128}), recomputing the
 probabilities from ``lse``.
+
+    y = io_aware_attention_gb300.bias_gelu_dropout(x, bias, keep, p)
+
+is the fused elementwise chain (bias add, tanh GELU, dropout with a packed
+keep mask drawn by the caller) in one HBM read and one write.
 """
 from __future__ import annotations
 
@@ -23,12 +28,12 @@ import os
 
 from . import _build
 
-__all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
+__all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "bias_gelu_dropout", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
            "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
-EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
+EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bias_gelu_dropout", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
            "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
 
 
@@ -64,6 +69,8 @@ def library():
     lib.fa_bwd.restype = ctypes.c_int
     lib.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
     lib.fa_bwd_workspace_bytes.restype = ctypes.c_int
+    lib.fa_bias_gelu_dropout.argtypes = [vp, vp, vp, vp, i64, i64, ctypes.c_float, vp]
+    lib.fa_bias_gelu_dropout.restype = ctypes.c_int
     lib.fa_decode.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_float, vp,
                               ctypes.c_size_t, vp]
     lib.fa_decode.restype = ctypes.c_int
@@ -191,6 +198,34 @@ def bwd(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, s
         ws = torch.empty(bwd_workspace_bytes(B, H, N, d), dtype=torch.uint8, device=q.device)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
         return bwd_into(q, k, v, o, lse, do, dq, dk, dv, ws, causal, scale, stream)
+
+
+def bias_gelu_dropout(x, bias, keep=None, p: float = 0.0, out=None, stream=None):
+    """y = dropout(gelu(x + bias)) for x (rows, cols) bf16 and bias (cols,) bf16
+    on the GPU; keep: int32/uint32 CUDA tensor of ceil(rows*cols/32) words of
+    keep bits (bit e % 32 of word e // 32 keeps flat element e), or None to
+    keep all; kept values are scaled by 1/(1-p).  Returns y (bf16, like x)."""
+    import torch
+
+    for name, t in (("x", x), ("bias", bias)):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+    if x.dim() != 2 or bias.shape != (x.shape[1],):
+        raise ValueError(f"x (rows, cols) and bias (cols,) expected: {tuple(x.shape)} {tuple(bias.shape)}")
+    rows, cols = (int(s) for s in x.shape)
+    if keep is not None:
+        if not keep.is_cuda or keep.dtype not in (torch.int32, torch.uint32) or not keep.is_contiguous():
+            raise ValueError("keep must be a contiguous CUDA int32/uint32 tensor of mask words")
+        if keep.numel() * 32 < rows * cols:
+            raise ValueError("keep holds fewer bits than x has elements")
+    y = torch.empty_like(x) if out is None else out
+    vp = ctypes.c_void_p
+    rc = library().fa_bias_gelu_dropout(vp(x.data_ptr()), vp(bias.data_ptr()),
+                                        vp(keep.data_ptr() if keep is not None else 0), vp(y.data_ptr()), rows,
+                                        cols, float(p), _stream_handle(stream))
+    if rc != 0:
+        raise FaError(rc, "fa_bias_gelu_dropout")
+    return y
 
 
 def _check_decode(q, k, v):

@@ -12,6 +12,7 @@
 #include "fa.h"
 #include "fa_bwd_kernel.cuh"
 #include "fa_decode_kernel.cuh"
+#include "fa_ew_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace {
@@ -153,6 +154,19 @@ struct BwdShape {
     int64_t BH, Np, num_kb, Dp;  // Dp: the kernel instance's (padded) head size
     size_t ws_bytes;
 };
+
+// Resident CTAs per SM of the elementwise kernel (cached per device).
+template <bool WIDE>
+int ew_ctas_per_sm(int dev)
+{
+    static std::atomic<int> cache[MAX_DEVICES];
+    if (dev < 0 || dev >= MAX_DEVICES) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fa::ew::fa_bias_gelu_dropout_kernel<WIDE>,
+                                                               fa::ew::THREADS, 0) == cudaSuccess)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 fa_status bwd_check(int64_t B, int64_t H, int64_t N, int64_t d, BwdShape* sh)
 {
@@ -522,6 +536,57 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     const int64_t n8 = BH * N * d / 8;
     fa::bwd::fa_bwd_dq_kernel<<<(unsigned)((n8 + 255) / 256), 256, 0, st>>>(
         acc, static_cast<__nv_bfloat16*>(dq), (int)N, (int)sh.Np, (int)d, (int)sh.Dp, n8, scale);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bias_gelu_dropout(const void* x, const void* bias, const uint32_t* keep, void* y, int64_t rows,
+                               int64_t cols, float p, fa_stream_t stream)
+{
+    // ---- argument checks (no CUDA call before these pass)
+    if (!x || !bias || !y) return FA_ERR_INVALID_ARG;
+    if (rows < 1 || cols < 1 || !(p >= 0.0f && p < 1.0f)) return FA_ERR_INVALID_ARG;
+    if (cols % 8 != 0) return FA_ERR_UNSUPPORTED;
+    if (rows > ((int64_t)1 << 62) / cols || cols / 8 > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(bias) |
+                          reinterpret_cast<uintptr_t>(y);
+    if ((mis & 15u) != 0 || (reinterpret_cast<uintptr_t>(keep) & 3u) != 0) return FA_ERR_UNSUPPORTED;
+    const int64_t n = rows * cols;
+    const size_t tb = (size_t)n * 2, bb = (size_t)cols * 2, kb = (size_t)((n + 31) / 32) * 4;
+    if (overlaps(y, tb, x, tb) || overlaps(y, tb, bias, bb) || (keep && overlaps(y, tb, keep, kb)))
+        return FA_ERR_INVALID_ARG;
+
+    int dev = -1;
+    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FA_ERR_CUDA;
+
+    fa::ew::Params prm;
+    prm.x = static_cast<const __nv_bfloat16*>(x);
+    prm.bias = static_cast<const __nv_bfloat16*>(bias);
+    prm.keep = reinterpret_cast<const uint8_t*>(keep);
+    prm.y = static_cast<__nv_bfloat16*>(y);
+    prm.n8 = n / 8;
+    prm.cols8 = (int)(cols / 8);
+    // Division by the invariant cols8 (Granlund and Montgomery's round-up
+    // method for 31-bit numerators): magic = floor(2^(31+l) / cols8) + 1.
+    int l = 0;
+    while (((int64_t)1 << l) < (int64_t)prm.cols8) ++l;
+    prm.magic = (uint32_t)((((uint64_t)1) << (31 + l)) / (uint64_t)prm.cols8 + 1);
+    prm.shift = 31 + l;
+    prm.scale = 1.0f / (1.0f - p);
+    // Exactly the CTAs that are resident at once (one wave), each thread
+    // keeping UNROLL 16-byte loads in flight, walking the tensor grid-stride.
+    const bool wide = prm.n8 >= ((int64_t)1 << 31);
+    const int per_sm = wide ? ew_ctas_per_sm<true>(dev) : ew_ctas_per_sm<false>(dev);
+    if (per_sm <= 0) return FA_ERR_CUDA;
+    const int64_t per_cta = (int64_t)fa::ew::THREADS * fa::ew::UNROLL;
+    const unsigned grid =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>((prm.n8 + per_cta - 1) / per_cta, (int64_t)per_sm * sms));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!wide)
+        fa::ew::fa_bias_gelu_dropout_kernel<false><<<grid, fa::ew::THREADS, 0, st>>>(prm);
+    else
+        fa::ew::fa_bias_gelu_dropout_kernel<true><<<grid, fa::ew::THREADS, 0, st>>>(prm);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -165,3 +165,45 @@ def sample_decode_rows(w: DecodeWorkload, n: int | None = None):
     if n >= 2:
         bh[1], row[1] = w.B * w.H - 1, w.Nq - 1
     return bh, row
+
+
+# ------------------------------------------------------- elementwise chain
+@dataclass(frozen=True)
+class EwWorkload:
+    """A bias + GELU + dropout problem: x (rows, cols), bias (cols,), keep mask
+    with keep probability 1 - p."""
+
+    name: str
+    rows: int
+    cols: int
+    p: float
+    seed: int
+
+
+EW_WORKLOADS = {
+    w.name: w
+    for w in [
+        # "Fusion and IO-aware kernels", § Why elementwise chains are pure
+        # traffic: the residual-stream activation (B, T, d) = (8, 4096, 4096)
+        # in bf16 (268 MB), here with bias + GELU + dropout; larger than L2.
+        EwWorkload("ew_b8_t4096_d4096_p0.1", 8 * 4096, 4096, 0.1, 3001),
+        # the 4096 x 8192 activation of the page's fusion.py byte count
+        EwWorkload("ew_4096x8192_p0.1", 4096, 8192, 0.1, 3002),
+    ]
+}
+
+
+def make_ew_inputs(rows: int, cols: int, p: float, seed: int, device="cpu"):
+    """Seeded x ~ N(0, 4) and bias ~ N(0, 1) in bf16, and a packed keep mask
+    (uint32 words as int32, bit e % 32 of word e // 32 keeps flat element e,
+    each kept with probability 1 - p) from numpy's default_rng(seed)."""
+    import torch
+
+    rng = np.random.default_rng(seed)
+    x = torch.from_numpy((rng.standard_normal((rows, cols), dtype=np.float32) * 2.0)).to(torch.bfloat16)
+    bias = torch.from_numpy(rng.standard_normal(cols, dtype=np.float32)).to(torch.bfloat16)
+    n = rows * cols
+    keep_bits = rng.random(((n + 31) // 32) * 32, dtype=np.float32) >= p
+    words = np.packbits(keep_bits.reshape(-1, 8), axis=1, bitorder="little").reshape(-1).view(np.uint32)
+    keep = torch.from_numpy(words.view(np.int32).copy())
+    return x.to(device), bias.to(device), keep.to(device)

@@ -157,3 +157,21 @@ def test_bwd_workspace_bytes(lib):
     assert lib.fa_bwd_workspace_bytes(1, 1, 64, 100, ctypes.byref(out)) == 2
     assert lib.fa_bwd_workspace_bytes(1, 1, 0, 128, ctypes.byref(out)) == 1
     assert lib.fa_bwd_workspace_bytes(1, 1, 64, 128, None) == 1
+
+
+def call_ew(lib, x=P, bias=2 * P, keep=3 * P, y=4 * P, rows=4, cols=64, p=0.1):
+    vp = ctypes.c_void_p
+    return lib.fa_bias_gelu_dropout(vp(x), vp(bias), vp(keep), vp(y), rows, cols, p, None)
+
+
+@pytest.mark.parametrize("kw, status", [
+    (dict(x=0), 1), (dict(bias=0), 1), (dict(y=0), 1), (dict(rows=0), 1), (dict(cols=-8), 1),
+    (dict(p=1.0), 1), (dict(p=-0.1), 1), (dict(p=float("nan")), 1),
+    (dict(cols=60), 2),                                   # cols not a multiple of 8
+    (dict(x=P + 8), 2), (dict(y=4 * P + 4), 2), (dict(keep=3 * P + 2), 2),
+    (dict(y=P + 64), 1),                                  # y overlaps x
+    (dict(keep=4 * P + 16), 1),                           # keep inside y
+    (dict(rows=1 << 40, cols=1 << 30), 1),                # element count overflows
+])
+def test_bad_ew_arguments_are_rejected(lib, kw, status):
+    assert call_ew(lib, **kw) == status
