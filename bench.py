@@ -55,7 +55,8 @@ DECODE_METRIC = "attention decode (split-KV): KV-cache bytes read per second"
 EW_METRIC = "fused bias+GELU+dropout (bf16): HBM bytes per second (x, bias, keep mask read once, y written once)"
 
 FWD_SOURCES = ("fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
-BWD_SOURCES = ('fa_bwd_kernel.cuh', 'fa_fwd_kernel.cuh', 'ptx.cuh', 'fa_api.cu')
+BWD_SOURCES = ("fa_bwd_kernel.cuh", "fa_fwd_kernel.cuh", "ptx.cuh", "fa_api.cu")
+EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 # DRAM bytes (read + write) per launch from one ncu capture, keyed by workload
 # name and pass, with the sha256 of the kernel sources it was taken on;
 # reported as roofline.traffic only while the sources still hash the same.
@@ -70,9 +71,14 @@ MEASURED_TRAFFIC = {
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "a21a7d994a7ac9b538fed68ce5fcb1d207b77bd5e80afc1b9f74176fe2700e75",
-        "bytes": 4 * (405_997_312 + 218_239_232),
+        "sha256": "d26f21087330fe31cae46586f2074eaed399ea0bd2326585770c1ed8eadf0458",
+        "bytes": 4 * (405_911_808 + 217_132_288),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
+    ("ew_b8_t4096_d4096_p0.1", "ew"): {
+        "sources": EW_SOURCES,
+        "sha256": "904d3532c0c483d90fe607216f912b7323ac4df26503284682ca281b546f74cc",
+        "bytes": 285_247_488 + 211_092_992,
+        "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

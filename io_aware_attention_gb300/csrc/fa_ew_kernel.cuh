@@ -86,8 +86,8 @@ __device__ __forceinline__ uint4 ld_stream(const void* p)
 }
 
 // Two neighbouring elements (a bf16 pair of x and of the bias, their two keep
-// bits) -> a bf16 pair of y.
-__device__ __forceinline__ uint32_t chain2(uint32_t xw, uint32_t bw, uint32_t bits, float scale)
+// bits as the pair's dropout factors {0 or 1/(1-p)} x 2) -> a bf16 pair of y.
+__device__ __forceinline__ uint32_t chain2(uint32_t xw, uint32_t bw, uint64_t fac)
 {
     const uint64_t x2 = ptx::f2_pack(__uint_as_float(xw << 16), __uint_as_float(xw & 0xFFFF0000u));
     const uint64_t b2 = ptx::f2_pack(__uint_as_float(bw << 16), __uint_as_float(bw & 0xFFFF0000u));
@@ -99,9 +99,6 @@ __device__ __forceinline__ uint32_t chain2(uint32_t xw, uint32_t bw, uint32_t bi
                                      ptx::f2_pack(1.0f, 1.0f));
     float d0, d1;
     ptx::f2_unpack(den, d0, d1);
-    const uint32_t s_bits = __float_as_uint(scale);
-    const uint64_t fac = ptx::f2_pack(__uint_as_float((0u - (bits & 1u)) & s_bits),
-                                      __uint_as_float((0u - ((bits >> 1) & 1u)) & s_bits));
     const uint64_t y = ptx::f2_mul(ptx::f2_mul(h, fac), ptx::f2_pack(rcp_approx(d0), rcp_approx(d1)));
     float y0, y1;
     ptx::f2_unpack(y, y0, y1);
@@ -111,6 +108,11 @@ __device__ __forceinline__ uint32_t chain2(uint32_t xw, uint32_t bw, uint32_t bi
 template <bool WIDE>
 __global__ void __launch_bounds__(THREADS, 4) fa_bias_gelu_dropout_kernel(const Params p)
 {
+    // Dropout factors of an element pair, indexed by its two keep bits.
+    __shared__ uint64_t ftab[4];
+    if (threadIdx.x < 4)
+        ftab[threadIdx.x] = ptx::f2_pack((threadIdx.x & 1u) ? p.scale : 0.0f, (threadIdx.x & 2u) ? p.scale : 0.0f);
+    __syncthreads();
     const int64_t per_round = (int64_t)gridDim.x * THREADS * UNROLL;
     for (int64_t v0 = (int64_t)blockIdx.x * THREADS * UNROLL + threadIdx.x; v0 < p.n8; v0 += per_round) {
         uint4 xv[UNROLL], bv[UNROLL];
@@ -128,12 +130,14 @@ __global__ void __launch_bounds__(THREADS, 4) fa_bias_gelu_dropout_kernel(const 
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t v = v0 + (int64_t)u * THREADS;
             if (v < p.n8) {
-                uint4 w;
-                w.x = chain2(xv[u].x, bv[u].x, kb[u], p.scale);
-                w.y = chain2(xv[u].y, bv[u].y, kb[u] >> 2, p.scale);
-                w.z = chain2(xv[u].z, bv[u].z, kb[u] >> 4, p.scale);
-                w.w = chain2(xv[u].w, bv[u].w, kb[u] >> 6, p.scale);
-                *reinterpret_cast<uint4*>(p.y + v * 8) = w;
+                const uint32_t w0 = chain2(xv[u].x, bv[u].x, ftab[kb[u] & 3u]);
+                const uint32_t w1 = chain2(xv[u].y, bv[u].y, ftab[(kb[u] >> 2) & 3u]);
+                const uint32_t w2 = chain2(xv[u].z, bv[u].z, ftab[(kb[u] >> 4) & 3u]);
+                const uint32_t w3 = chain2(xv[u].w, bv[u].w, ftab[(kb[u] >> 6) & 3u]);
+                // Streaming store: y is not read again by this kernel.
+                asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p.y + v * 8), "r"(w0), "r"(w1),
+                             "r"(w2), "r"(w3)
+                             : "memory");
             }
         }
     }
