@@ -26,8 +26,8 @@
 //              lane quarter) and score columns 64*(w/4) .. +63, so every SM
 //              sub-partition runs two softmax warps (w and w+4, the two halves
 //              of the same rows).  Each thread owns half a row: masking,
-//              partial row max (exchanged with the partner warp through shared
-//              memory and a 64-thread named barrier), exponentials, its half of
+//              partial row max (exchanged with the partner warp through TMEM
+//              and a 64-thread named barrier), exponentials, its half of
 //              P, its half of the O columns for rescaling, and the epilogue of
 //              those columns (straight from registers to global memory).
 //   warp 8     TMA producer: Q once per item, K_j / V_j into rings of stages,
@@ -44,6 +44,7 @@
 //   [256,256+d) O (fp32)     [256+d, 256+d+16) l~ (16 equal copies)
 //   [400,464) P (bf16 pairs, one tile)
 //   [464,466) the two halves' fp32 row sums, exchanged in the epilogue
+//   [468,472) the two halves' row maxima of a tile, per S buffer
 // S_{j+2} goes into S_j's buffer as soon as every softmax warp has read S_j
 // into registers (S_READ); P_j goes into the P buffer once P_{j-1} V_{j-1} is
 // complete (O_DONE).  So the score stream runs ahead of the P.V stream and
@@ -85,7 +86,7 @@ constexpr int WARP_MMA_S = 9;
 constexpr int WARP_MMA_O = 10;
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t WAIT_SLEEP_NS = 20000;  // suspend-time hint of one poll
-constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P = 400, TM_LX = 464;
+constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P = 400, TM_LX = 464, TM_MX = 468;
 constexpr uint32_t TM_COLS = 512;
 constexpr uint32_t BLK_BYTES = BN * 128;  // one 64-column, 128-row swizzled block (16 KB)
 
@@ -115,16 +116,15 @@ struct Layout {
     static constexpr int VSTAGES = (D == 128) ? 2 : 4;
     static constexpr int DBLK = D / 64;                   // 64-column blocks of a row
     static constexpr uint32_t TM_L = TM_O + D;            // l~ columns
-    static_assert(TM_L + 16 <= TM_P && TM_P + 64 <= TM_LX && TM_LX + 2 <= TM_COLS, "TMEM budget");
+    static_assert(TM_L + 16 <= TM_P && TM_P + 64 <= TM_LX && TM_LX + 2 <= TM_MX && TM_MX + 4 <= TM_COLS,
+                  "TMEM budget");
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;      // bytes of one K or V tile
     static constexpr uint32_t VSTAGE = (DBLK + 1) * BLK_BYTES;  // V blocks + the ones block
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KSTAGES * KV_BYTES;
-    static constexpr uint32_t OFF_RED = OFF_V + VSTAGES * VSTAGE;  // float[2 slots][2 halves][BM]
-    static constexpr uint32_t RED_BYTES = 4 * BM * 4;
-    static constexpr uint32_t OFF_BAR = OFF_RED + RED_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + VSTAGES * VSTAGE;
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
     static constexpr int B_KFULL = 2;
@@ -297,7 +297,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     volatile uint32_t* const misc = reinterpret_cast<volatile uint32_t*>(sgen + L::OFF_MISC);
     volatile uint32_t* const abort_flag = misc + 1;
-    float* const red = reinterpret_cast<float*>(sgen + L::OFF_RED);  // [2 slots][2 halves][BM]
     auto bar = [&](int i) -> uint32_t { return sbase + L::OFF_BAR + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -607,13 +606,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
                     }
                     mx = max64(sr);
-                    red[(b * 2 + half) * BM + row] = mx;
+                    ptx::tmem_st1(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + half), __float_as_uint(mx));
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before_sync();
                 }
-                // Row max: this half's, then the partner warp's through shared memory.
+                // Row max: this half's, then the partner warp's through two TMEM
+                // columns per S buffer (TMEM, unlike shared memory, does not
+                // queue behind the score MMAs' operand reads).  The slot is
+                // rewritten two tiles later, after the partner has passed the
+                // next tile's barrier, so after it read this value.
                 ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
                 if (lane == 0) FA_TRACE_EV(warp, g, 2);
                 if (!ok) continue;
-                mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * BM + row]);
+                ptx::tc_fence_after_sync();
+                mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1_wait(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + (half ^ 1)))));
                 const float m_tile = mx * sl2;  // scale > 0, so max commutes with it
 
                 // [O | l~] and the P buffer are free of tile g - 1 once its P.V

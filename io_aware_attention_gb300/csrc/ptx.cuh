@@ -443,6 +443,17 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
+// One TMEM column of this warp's 32 lanes, loaded and waited for in one step.
+__device__ __forceinline__ uint32_t tmem_ld1_wait(uint32_t taddr)
+{
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+                 : "=r"(v)
+                 : "r"(taddr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t& a, uint32_t& b)
 {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(taddr));
