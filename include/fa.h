@@ -256,11 +256,12 @@ fa_status fa_set_wait_limit_ns(uint64_t ns);
 
 /*
  * fa_debug_skip_k_tile — test hook for the failure path.  With tile >= 0, the
- * first CTA of every later launch never loads its tile-th K tile, so the MMA
- * warp's wait for it runs out after the wait limit, the kernel abandons its
- * work and fa_check_device_status reports FA_ERR_TIMEOUT; no fault, trap or
- * hang is involved.  -1 (the default) turns it off.  Outputs of a launch made
- * with the hook on are incomplete.
+ * first CTA of every later fa_fwd launch never loads its tile-th K tile, and
+ * that of every later fa_bwd launch never loads the Q / dout tile of its
+ * tile-th step, so the MMA warp's wait for it runs out after the wait limit,
+ * the kernel abandons its work and fa_check_device_status reports
+ * FA_ERR_TIMEOUT; no fault, trap or hang is involved.  -1 (the default) turns
+ * it off.  Outputs of a launch made with the hook on are incomplete.
  */
 fa_status fa_debug_skip_k_tile(int tile);
 

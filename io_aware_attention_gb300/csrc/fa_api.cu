@@ -522,6 +522,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.scale = scale;
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    p.debug_skip_q = g_debug_skip_k.load(std::memory_order_relaxed);
     const unsigned grid = (unsigned)std::min<int64_t>((BH * sh.num_kb + 1) / 2, sms);
     fa_status ms;
     if (sh.Dp == 128)

@@ -82,7 +82,12 @@
 // on expiry the CTA records the wait in the device status word and raises an
 // abort flag, after which the roles keep walking their loops (skipping the
 // work, still meeting the named barriers), drain in-flight copies / MMAs and
-// reach the common exit, where TMEM is freed.
+// reach the common exit, where TMEM is freed.  An aborted producer signals
+// with bar.sync rather than bar.arrive (nb_signal), so it cannot run a
+// generation ahead of the issuer; the issuer meets each producer group's
+// barriers in the order that group signals them (P_READY, DP_READ, DS_READY
+// per step; DQ_READ per step, then ACC_READ per item), so those syncs cannot
+// wait on one another in a cycle.
 #pragma once
 
 #include <cuda.h>
@@ -107,20 +112,36 @@ constexpr uint32_t TM_S0 = 0, TM_S1 = 64, TM_DP = 128, TM_DQ = 192, TM_DV = 256,
 constexpr uint32_t TM_COLS = 512;
 
 // Named barriers (0 is __syncthreads).  P/dS warps -> issuer: 256 + 32
-// threads; dQ warps -> issuer: 128 + 32.  P_READY and DS_READY alternate
-// between two ids by step parity: the P/dS warps may run one step ahead.
+// threads; dQ warps -> issuer: 128 + 32.  Each alternates between two ids by
+// the parity of its step (or item): see nb_signal.
 constexpr uint32_t NB_P_READY = 1;    // + (g & 1): P(g) in TMEM
 constexpr uint32_t NB_DS_READY = 3;   // + (g & 1): dS(g) in shared memory
-constexpr uint32_t NB_DP_READ = 5;    // dP(g) read out of TMEM (so dP(g) is complete)
-constexpr uint32_t NB_DQ_READ = 6;    // dQ(g) read out of TMEM
-constexpr uint32_t NB_ACC_READ = 7;   // dK, dV of an item read out of TMEM
+constexpr uint32_t NB_DP_READ = 5;    // + (g & 1): dP(g) read out of TMEM (so dP(g) is complete)
+constexpr uint32_t NB_DQ_READ = 7;    // + (g & 1): dQ(g) read out of TMEM
+constexpr uint32_t NB_ACC_READ = 9;   // + (k & 1): dK, dV of item k read out of TMEM
 constexpr uint32_t NB_PDS_COUNT = 32 * PDS_WARPS + 32;
 constexpr uint32_t NB_DQ_COUNT = 32 * 4 + 32;
 
-__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count)
+// Producer side of a producer -> issuer named barrier; the issuer meets every
+// generation with bar.sync, in order.  While the pipeline runs, the producer
+// only arrives (bar.arrive does not wait), and the mbarrier it waited on
+// before signalling generation n + 1 guarantees that generation n has
+// completed.  After an abort those waits are skipped, so the producer joins
+// with bar.sync instead.  A signal alternates between two ids by generation
+// parity: then a producer's next arrival on an id, two generations later,
+// always finds the earlier generation complete -- by the mbarrier wait, or
+// by the bar.sync it went through in between -- even when it switched from
+// arriving to syncing in between.  (On one id, an aborted producer's sync
+// could land on a generation that its own earlier arrival has not seen
+// complete yet.)
+__device__ __forceinline__ void nb_signal(uint32_t id, uint32_t count, bool ok)
 {
-    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+    if (ok)
+        ptx::named_barrier_arrive(id, count);
+    else
+        ptx::named_barrier_sync(id, count);
 }
+
 
 struct Params {
     __nv_bfloat16* dk;
@@ -136,6 +157,7 @@ struct Params {
     float scale_log2;
     float scale;
     unsigned long long wait_limit_ns;
+    int debug_skip_q;  // test hook: global step whose Q/dO tile the first CTA never loads (-1: none)
 };
 
 template <int D>
@@ -279,7 +301,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!(ok = warp_wait_bar(bar(L::B_QEMPTY + s), ((uint32_t)(g / QSTAGES) & 1u) ^ 1u, limit,
                                          abort_flag, 0x1100 + L::B_QEMPTY + s)))
                     break;
-                if (ptx::elect_one()) {
+                // Test hook: the first CTA leaves one step's tile unloaded, so
+                // the issuer's wait for it runs out (exercises the abort path).
+                if (ptx::elect_one() && !(g == p.debug_skip_q && blockIdx.x == 0)) {
                     const int q0 = (it.m0 + t) * BQ;
                     const uint32_t fb = bar(L::B_QFULL + s);
                     ptx::mbar_arrive_expect_tx(fb, 2 * L::QT_BYTES);
@@ -294,7 +318,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Drain: every copy this warp issued lands before exit.
         if (k > 0) drain_bar(bar(L::B_KVFULL), (uint32_t)((k - 1) & 1), limit, abort_flag, 0x1180);
         for (int gg = max(0, g - QSTAGES); gg < g; ++gg)
-            drain_bar(bar(L::B_QFULL + gg % QSTAGES), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag, 0x1181);
+            if (!(gg == p.debug_skip_q && blockIdx.x == 0))
+                drain_bar(bar(L::B_QFULL + gg % QSTAGES), (uint32_t)(gg / QSTAGES) & 1u, limit, abort_flag, 0x1181);
     } else if (warp == WARP_MMA) {
         // ----------------------------------------------------- MMA issuer
         constexpr uint32_t ID_S = ptx::idesc_bf16_f32_ab(BKV, BQ, false, false);  // S^T, dP^T
@@ -347,15 +372,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const Item it = item_of<CAUSAL>(i, p);
             if (ok) ok = warp_wait_bar(bar(L::B_KVFULL), (uint32_t)(k & 1), limit, abort_flag, 0x1200 + L::B_KVFULL);
-            if (g >= 1) ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);  // dP(g-1) read
             issue_s_dp(g);
             for (int t = 0; t < it.nq; ++t, ++g) {
                 const int s = g % QSTAGES, b = g & 1;
                 const bool more = t + 1 < it.nq;
                 // dV += P^T dO: A = P^T from TMEM (bf16 pairs; queries 16kk.. at
                 // column 32*(kk/2) + 8*(kk%2) of the S buffer), B = dO MN-major.
-                // The first of an item overwrites dV: the epilogue has read it.
-                if (t == 0 && k > 0) ptx::named_barrier_sync(NB_ACC_READ, NB_DQ_COUNT);
+                // The first of an item overwrites dV: the epilogue has read it
+                // (the dQ warps read the previous item's last dQ before that).
+                if (t == 0 && k > 0) {
+                    ptx::named_barrier_sync(NB_DQ_READ + (uint32_t)((g - 1) & 1), NB_DQ_COUNT);
+                    ptx::named_barrier_sync(NB_ACC_READ + (uint32_t)((k - 1) & 1), NB_DQ_COUNT);
+                }
                 ptx::named_barrier_sync(NB_P_READY + (uint32_t)b, NB_PDS_COUNT);
                 if (ok) {
                     ptx::tc_fence_after_sync();
@@ -367,10 +395,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         do_mn + off(s * L::QT_BYTES + kk * 2048), ID_G, (t > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                if (more) {
-                    ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);  // dP(g) read
-                    issue_s_dp(g + 1);
-                }
+                ptx::named_barrier_sync(NB_DP_READ + (uint32_t)b, NB_PDS_COUNT);  // dP(g) read
+                if (more) issue_s_dp(g + 1);
                 // dK += dS^T Q: A = dS^T K-major, B = Q MN-major.
                 ptx::named_barrier_sync(NB_DS_READY + (uint32_t)b, NB_PDS_COUNT);
                 if (ok) {
@@ -385,8 +411,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (ptx::elect_one()) ptx::tc_commit(bar(L::B_QEMPTY + s));
                 }
                 // dQ^T = K^T dS^T: A = K MN-major, B = dS^T MN-major, once the
-                // dQ warps have read dQ(g - 1) out of TMEM.
-                if (g >= 1) ptx::named_barrier_sync(NB_DQ_READ, NB_DQ_COUNT);
+                // dQ warps have read dQ(g - 1) out of TMEM (at an item's first
+                // step, met above).
+                if (t > 0) ptx::named_barrier_sync(NB_DQ_READ + (uint32_t)((g - 1) & 1), NB_DQ_COUNT);
                 if (ok) {
                     ptx::tc_fence_after_sync();
 #pragma unroll
@@ -405,12 +432,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
-        // The last step's signals, so that every named barrier completes.
-        if (g >= 1) {
-            ptx::named_barrier_sync(NB_DP_READ, NB_PDS_COUNT);
-            ptx::named_barrier_sync(NB_DQ_READ, NB_DQ_COUNT);
+        // The last item's signals, so that every named barrier completes.
+        if (k >= 1) {
+            ptx::named_barrier_sync(NB_DQ_READ + (uint32_t)((g - 1) & 1), NB_DQ_COUNT);
+            ptx::named_barrier_sync(NB_ACC_READ + (uint32_t)((k - 1) & 1), NB_DQ_COUNT);
         }
-        if (k >= 1) ptx::named_barrier_sync(NB_ACC_READ, NB_DQ_COUNT);
         if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
         drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x1280);
     } else if (warp >= WARP_DQ0) {
@@ -436,7 +462,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::reg_fence(c);
                     ptx::tc_fence_before_sync();
                     __syncwarp();
-                    nb_arrive(NB_DQ_READ, NB_DQ_COUNT);
+                    nb_signal(NB_DQ_READ + (uint32_t)(g & 1), NB_DQ_COUNT, ok);
                     // The staging block is free once this warp's previous reduce
                     // has read it.  Row q holds this warp's 32 head dims of query q.
                     if (lane == 0) ptx::tma_store_wait_read();
@@ -455,7 +481,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {
                     __syncwarp();
-                    nb_arrive(NB_DQ_READ, NB_DQ_COUNT);
+                    nb_signal(NB_DQ_READ + (uint32_t)(g & 1), NB_DQ_COUNT, ok);
                 }
             }
             // Epilogue: dV and scale * dK of this warp's 32 keys, bf16.
@@ -489,7 +515,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tc_fence_before_sync();
             }
             __syncwarp();
-            nb_arrive(NB_ACC_READ, NB_DQ_COUNT);
+            nb_signal(NB_ACC_READ + (uint32_t)(k & 1), NB_DQ_COUNT, ok);
         }
         // Every reduce this warp issued completes before exit.
         if (lane == 0) ptx::bulk_wait_all();
@@ -553,7 +579,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_before_sync();
                 }
                 __syncwarp();
-                nb_arrive(NB_P_READY + (uint32_t)b, NB_PDS_COUNT);
+                nb_signal(NB_P_READY + (uint32_t)b, NB_PDS_COUNT, ok);
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) d4[c4] = __ldg(drow + c4);
 
@@ -571,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tc_fence_before_sync();
                 }
                 __syncwarp();
-                nb_arrive(NB_DP_READ, NB_PDS_COUNT);
+                nb_signal(NB_DP_READ + (uint32_t)b, NB_PDS_COUNT, ok);
                 if (ok) {
                     // dS = P (dP - D), bf16 pairs, into dS^T buffer b (row r,
                     // bytes 64*half .. +63, 128-byte swizzle: 16-byte chunk c of
@@ -596,7 +622,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::fence_proxy_async_smem();
                 }
                 __syncwarp();
-                nb_arrive(NB_DS_READY + (uint32_t)b, NB_PDS_COUNT);
+                nb_signal(NB_DS_READY + (uint32_t)b, NB_PDS_COUNT, ok);
             }
         }
     }

@@ -179,6 +179,12 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrives at a named barrier without waiting for it (the producer side).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // --------------------------------------------------------- tcgen05 / TMEM
 
 // Allocates `ncols` TMEM columns (power of two, >= 32); the base address is

@@ -1,0 +1,205 @@
+"""Model check of the backward kernel's producer -> issuer named-barrier
+protocol, aborts included (CPU only).
+
+The kernel's roles are replayed as coroutines under random interleavings, with
+the hardware's named-barrier rule: a barrier id counts arriving warps, and
+when the count reaches the expected number it completes, releases the warps
+blocked in bar.sync on it and starts over.  A warp that arrives again on an
+id whose current generation already holds its arrival would be counted into
+the wrong generation (an overrun); a state in which every live warp is blocked
+is a deadlock.  mbarrier waits (the MMA-completion and TMA signals) succeed
+once their event has happened, fail at once after an abort, and may time out
+(raising the abort) at any point before.
+
+Checked: with the kernel's rules -- every signal alternating between two ids
+by generation parity, a producer arriving while healthy and joining with
+bar.sync after an abort, the issuer meeting each producer group's barriers in
+the order that group signals them -- no interleaving overruns or deadlocks,
+whatever waits time out.  The same protocol on a single id per signal does
+overrun, which shows that the check can fail.
+"""
+import random
+
+import pytest
+
+
+class Deadlock(Exception):
+    pass
+
+
+class Overrun(Exception):
+    pass
+
+
+def simulate(roles, expected, seed, p_timeout):
+    """Runs the coroutines `roles` ({name: generator}) to the end under one
+    random schedule.  Yields from a role: ('emit', ev), ('wait', ev) -> bool,
+    ('arrive', id), ('sync', id).  Returns whether an abort happened."""
+    rng = random.Random(seed)
+    events, bars = set(), {}
+    aborted = False
+    state = {n: ("ready", None) for n in roles}
+    live = set(roles)
+    while live:
+        choices = []
+        for n in live:
+            kind, arg = state[n]
+            if kind == "ready":
+                choices.append(n)
+            elif kind == "wait" and (arg in events or aborted or rng.random() < p_timeout):
+                choices.append(n)
+        if not choices:
+            waiting = [n for n in live if state[n][0] == "wait"]
+            if not waiting:
+                raise Deadlock({n: state[n] for n in live})
+            choices = waiting  # only a timeout can move on
+        n = rng.choice(choices)
+        kind, arg = state[n]
+        send = None
+        if kind == "wait":
+            if arg in events:
+                send = True
+            else:
+                aborted, send = True, False
+        try:
+            act = roles[n].send(send)
+        except StopIteration:
+            live.discard(n)
+            state[n] = ("done", None)
+            continue
+        if act[0] == "emit":
+            events.add(act[1])
+            state[n] = ("ready", None)
+        elif act[0] == "wait":
+            state[n] = ("wait", act[1])
+        else:
+            count, members, blocked = bars.setdefault(act[1], [0, set(), []])
+            if n in members:
+                raise Overrun((n, act[1]))
+            bar = bars[act[1]]
+            bar[0] += 1
+            members.add(n)
+            if act[0] == "sync":
+                blocked.append(n)
+                state[n] = ("blocked", act[1])
+            else:
+                state[n] = ("ready", None)
+            if bar[0] == expected(act[1]):
+                for m in blocked:
+                    state[m] = ("ready", None)
+                bars[act[1]] = [0, set(), []]
+    for bid, (count, _, _) in bars.items():
+        if count:
+            raise Deadlock(("generation left open", bid, count))
+    return aborted
+
+
+def backward_roles(items, two_ids=True):
+    """The backward kernel's roles for one CTA walking `items` (query steps
+    per work item): the MMA issuer, the TMA producer, 8 P/dS warps and 4 dQ
+    warps, with the named barriers P_READY, DP_READ, DS_READY (P/dS warps ->
+    issuer), DQ_READ and ACC_READ (dQ warps -> issuer)."""
+    par = (lambda n: n & 1) if two_ids else (lambda n: 0)
+
+    def signal(ok, name, n):
+        return ("arrive" if ok else "sync", (name, par(n)))
+
+    def issuer():
+        ok, g = True, 0
+
+        def issue_s_dp(gg):
+            nonlocal ok
+            if ok:
+                ok = yield ("wait", ("QFULL", gg))
+            if ok:
+                yield ("emit", ("SFULL", gg))
+                yield ("emit", ("DPFULL", gg))
+
+        for k, nq in enumerate(items):
+            if ok:
+                ok = yield ("wait", ("KVFULL", k))
+            yield from issue_s_dp(g)
+            for t in range(nq):
+                more = t + 1 < nq
+                if t == 0 and k > 0:
+                    yield ("sync", ("DQ_READ", par(g - 1)))
+                    yield ("sync", ("ACC_READ", par(k - 1)))
+                yield ("sync", ("P_READY", par(g)))
+                yield ("sync", ("DP_READ", par(g)))
+                if more:
+                    yield from issue_s_dp(g + 1)
+                yield ("sync", ("DS_READY", par(g)))
+                if t > 0:
+                    yield ("sync", ("DQ_READ", par(g - 1)))
+                if ok:
+                    yield ("emit", ("DQFULL", g))
+                    if not more:
+                        yield ("emit", ("ACCFULL", k))
+                g += 1
+        if items:
+            yield ("sync", ("DQ_READ", par(g - 1)))
+            yield ("sync", ("ACC_READ", par(len(items) - 1)))
+
+    def tma():
+        for k in range(len(items)):
+            yield ("emit", ("KVFULL", k))
+        for g in range(sum(items)):
+            yield ("emit", ("QFULL", g))
+
+    def pds():
+        ok, g = True, 0
+        for nq in items:
+            for _ in range(nq):
+                if ok:
+                    ok = yield ("wait", ("SFULL", g))
+                yield signal(ok, "P_READY", g)
+                if ok:
+                    ok = yield ("wait", ("DPFULL", g))
+                yield signal(ok, "DP_READ", g)
+                yield signal(ok, "DS_READY", g)
+                g += 1
+
+    def dq():
+        ok, g = True, 0
+        for k, nq in enumerate(items):
+            for _ in range(nq):
+                if ok:
+                    ok = yield ("wait", ("DQFULL", g))
+                yield signal(ok, "DQ_READ", g)
+                g += 1
+            if ok:
+                ok = yield ("wait", ("ACCFULL", k))
+            yield signal(ok, "ACC_READ", k)
+
+    roles = {"issuer": issuer(), "tma": tma()}
+    roles.update({f"pds{i}": pds() for i in range(8)})
+    roles.update({f"dq{i}": dq() for i in range(4)})
+    return roles
+
+
+def expected(bid):
+    return 9 if bid[0] in ("P_READY", "DP_READ", "DS_READY") else 5  # producer warps + the issuer
+
+
+def cases(n):
+    rng = random.Random(12345)
+    for seed in range(n):
+        items = [rng.randint(1, 4) for _ in range(rng.randint(1, 4))]
+        yield seed, items, rng.choice([0.0, 0.001, 0.01, 0.05, 0.3])
+
+
+def test_backward_protocol_never_overruns_or_deadlocks():
+    aborted = clean = 0
+    for seed, items, p in cases(600):
+        if simulate(backward_roles(items), expected, seed, p):
+            aborted += 1
+        else:
+            clean += 1
+    assert aborted > 100 and clean > 100  # both paths were exercised
+
+
+def test_single_id_per_signal_overruns_after_an_abort():
+    with pytest.raises(Overrun):
+        for seed, items, p in cases(600):
+            if p > 0:
+                simulate(backward_roles(items, two_ids=False), expected, seed, p)
