@@ -122,26 +122,8 @@ constexpr uint32_t NB_ACC_READ = 9;   // + (k & 1): dK, dV of item k read out of
 constexpr uint32_t NB_PDS_COUNT = 32 * PDS_WARPS + 32;
 constexpr uint32_t NB_DQ_COUNT = 32 * 4 + 32;
 
-// Producer side of a producer -> issuer named barrier; the issuer meets every
-// generation with bar.sync, in order.  While the pipeline runs, the producer
-// only arrives (bar.arrive does not wait), and the mbarrier it waited on
-// before signalling generation n + 1 guarantees that generation n has
-// completed.  After an abort those waits are skipped, so the producer joins
-// with bar.sync instead.  A signal alternates between two ids by generation
-// parity: then a producer's next arrival on an id, two generations later,
-// always finds the earlier generation complete -- by the mbarrier wait, or
-// by the bar.sync it went through in between -- even when it switched from
-// arriving to syncing in between.  (On one id, an aborted producer's sync
-// could land on a generation that its own earlier arrival has not seen
-// complete yet.)
-__device__ __forceinline__ void nb_signal(uint32_t id, uint32_t count, bool ok)
-{
-    if (ok)
-        ptx::named_barrier_arrive(id, count);
-    else
-        ptx::named_barrier_sync(id, count);
-}
-
+// The producer warps signal with nb_signal (the forward kernel's header):
+// bar.arrive while healthy, bar.sync after an abort.
 
 struct Params {
     __nv_bfloat16* dk;

@@ -48,7 +48,8 @@
 // S_{j+2} goes into S_j's buffer as soon as every softmax warp has read S_j
 // into registers (S_READ); P_j goes into the P buffer once P_{j-1} V_{j-1} is
 // complete (O_DONE).  So the score stream runs ahead of the P.V stream and
-// neither issuer waits for the other.
+// neither issuer waits for the other.  The score issuer hands "S_j written"
+// to the softmax warps through a named barrier (see its loop).
 //
 // l~ = rowsum(bf16(P)): each V stage carries a 64-wide block of ones after
 // its d value columns, and the P.V MMA runs with N = d + 16, so the tensor
@@ -63,9 +64,12 @@
 // TMA boxes are 64 columns wide and fill columns past d with zeros, which add
 // nothing to any dot product; the epilogue stores d columns with row stride d.
 //
-// Every wait is bounded in time; on expiry the thread records the wait in the
-// device status word, raises a CTA-wide abort flag, and all roles drain their
-// in-flight copies / MMAs and reach the common exit, where TMEM is freed.
+// Every mbarrier wait is bounded in time; on expiry the thread records the
+// wait in the device status word, raises a CTA-wide abort flag, and all roles
+// drain their in-flight copies / MMAs and reach the common exit, where TMEM is
+// freed.  Named barriers are counted, not timed: the roles that meet them
+// (score issuer, softmax warps) walk every item and tile also after an abort,
+// skipping the work, so every generation completes.
 #pragma once
 
 #include <cuda.h>
@@ -94,8 +98,34 @@ constexpr uint32_t STATUS_TIMEOUT = 1u;
 constexpr uint32_t STATUS_BAD_SMEM = 2u;
 
 // Named barriers (0 is __syncthreads): 1..4 pair the two softmax warps of a
-// lane quarter.
+// lane quarter; 5..7 carry "S of tile g is in TMEM" from the score MMA issuer
+// to the softmax warps, id 5 + g % 3 (see nb_signal: the score stream runs
+// two tiles ahead, so a generation's id may come round again only after two
+// others).
 constexpr uint32_t NB_PAIR0 = 1;
+constexpr uint32_t NB_SREADY0 = 5;  // + (g % 3)
+constexpr uint32_t NB_SREADY_COUNT = SOFTMAX_THREADS + 32;
+
+// Producer side of a producer -> consumers named barrier; the consumers meet
+// every generation with bar.sync, in order.  While the pipeline runs, the
+// producer only arrives (bar.arrive does not wait), and the mbarrier it
+// waited on before signalling generation n guarantees that generation n - P
+// has completed (P, the pacing depth, is 1 for the backward's signals and 2
+// for the forward's S-ready signal).  After an abort those waits are
+// skipped, so the producer joins with bar.sync instead.  Generation n uses id
+// base + n % (P + 1): then, when the producer arrives for generation n, the
+// generation that last used the id, n - P - 1, has completed -- through the
+// mbarrier wait of the arrival before, or through the bar.sync it went
+// through -- even when it switched from arriving to syncing in between.
+// (With fewer ids, an aborted producer's sync could land on a generation
+// that its own earlier arrival has not seen complete yet.)
+__device__ __forceinline__ void nb_signal(uint32_t id, uint32_t count, bool ok)
+{
+    if (ok)
+        ptx::named_barrier_arrive(id, count);
+    else
+        ptx::named_barrier_sync(id, count);
+}
 
 struct Params {
     __nv_bfloat16* o;
@@ -456,24 +486,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr uint32_t IDESC_S = ptx::idesc_bf16_f32(BM, BN, false);
         const uint64_t q_desc = ptx::sdesc_sw128(sbase + L::OFF_Q, 16, 1024);
         const uint64_t k_desc0 = ptx::sdesc_sw128(sbase + L::OFF_K, 16, 1024);
+        //
+        // This warp also tells the softmax warps that S of a tile is complete:
+        // it waits on the MMA completion (an mbarrier) long before they need
+        // it and arrives on a named barrier, which they meet in a few cycles.
+        // An mbarrier poll of theirs would queue in shared memory behind the
+        // score MMAs' operand reads (hundreds of cycles on every tile).  S of
+        // tile g - 1 is signalled before the waits for tile g, so a new item's
+        // Q load never delays the last tile of the previous item.  The loops
+        // walk every item and tile also after an abort (the MMAs are skipped),
+        // so that every S-ready generation is signalled.
         int g = 0, k = 0;  // tiles and items done
         bool ok = true;
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+        auto signal_s_ready = [&](int gg) {
+            if (ok) ok = warp_wait_bar(bar(L::B_SFULL + (gg & 1)), (uint32_t)(gg >> 1) & 1u, limit, abort_flag,
+                                       0x200 + L::B_SFULL + (gg & 1));
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            nb_signal(NB_SREADY0 + (uint32_t)(gg % 3), NB_SREADY_COUNT, ok);
+        };
+        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const int n = item_of<CAUSAL>(i, p).n_kv;
-            if (!(ok = warp_wait_bar(bar(L::B_QFULL), (uint32_t)(k & 1), limit, abort_flag, 0x200 + L::B_QFULL)))
-                break;
             for (int j = 0; j < n; ++j, ++g) {
                 const int b = g & 1;
                 const int s = g % L::KSTAGES;
+                if (g >= 1) signal_s_ready(g - 1);
+                if (j == 0 && ok)
+                    ok = warp_wait_bar(bar(L::B_QFULL), (uint32_t)(k & 1), limit, abort_flag, 0x200 + L::B_QFULL);
+                // K of tile g was loaded long before: its check goes first, the
+                // wait for the softmax warps' signal last.
+                if (ok) ok = warp_wait_bar(bar(L::B_KFULL + s), (uint32_t)(g / L::KSTAGES) & 1u, limit, abort_flag,
+                                           0x200 + L::B_KFULL + s);
                 // Buffer b is free once every softmax warp has read S of tile
                 // g - 2 (the phase before cannot alias: S of g - 2 was issued
                 // only after S of g - 4 had been read).
-                if (g >= 2 && !(ok = warp_wait_bar(bar(L::B_SREAD + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
-                                                   abort_flag, 0x200 + L::B_SREAD + b)))
-                    break;
-                if (!(ok = warp_wait_bar(bar(L::B_KFULL + s), (uint32_t)(g / L::KSTAGES) & 1u, limit,
-                                         abort_flag, 0x200 + L::B_KFULL + s)))
-                    break;
+                if (g >= 2 && ok) ok = warp_wait_bar(bar(L::B_SREAD + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
+                                                     abort_flag, 0x200 + L::B_SREAD + b);
+                if (!ok) continue;
                 if (lane == 0) FA_TRACE_EV(9, g, 0);
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem + (b ? TM_S1 : TM_S0);
@@ -493,6 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        if (g >= 1) signal_s_ready(g - 1);
         // Drain: all MMAs issued by this warp complete before TMEM is freed.
         if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN));
         drain_bar(bar(L::B_DRAIN), 0, limit, abort_flag, 0x280);
@@ -516,16 +566,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             for (int j = 0; j < n; ++j, ++g) {
                 const int s = g % L::VSTAGES;
-                // P of tile g (the phase before is P of g - 1, which this warp
-                // has consumed, so parity cannot alias).
-                if (!(ok = warp_wait_bar(bar(L::B_PFULL), (uint32_t)(g & 1), limit, abort_flag,
-                                         0x200 + L::B_PFULL)))
-                    break;
-                if (lane == 0) FA_TRACE_EV(10, g, 2);
+                // V of tile g, loaded long before, is checked first: an mbarrier
+                // check is slow while the score MMAs stream their operands, and
+                // it then overlaps the softmax warps' work on P.  Then P of tile
+                // g (the phase before is P of g - 1, which this warp has
+                // consumed, so parity cannot alias).
                 if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
                                          abort_flag, 0x200 + L::B_VFULL + s)))
                     break;
                 if (lane == 0) FA_TRACE_EV(10, g, 3);
+                if (!(ok = warp_wait_bar(bar(L::B_PFULL), (uint32_t)(g & 1), limit, abort_flag,
+                                         0x200 + L::B_PFULL)))
+                    break;
+                if (lane == 0) FA_TRACE_EV(10, g, 2);
                 ptx::tc_fence_after_sync();
                 const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
 #pragma unroll
@@ -580,13 +633,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
             for (int j = 0; j < it.n_kv; ++j, ++g) {
                 const int b = g & 1;
+                // S of tile g is in TMEM (met on every tile, also after an abort).
+                ptx::named_barrier_sync(NB_SREADY0 + (uint32_t)(g % 3), NB_SREADY_COUNT);
                 if (ok) {
-                    ok = warp_wait_bar(bar(L::B_SFULL + b), (uint32_t)(g >> 1) & 1u, limit, abort_flag,
-                                       0x300 + L::B_SFULL + b);
-                    if (ok) {
-                        ptx::tc_fence_after_sync();
-                        ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
-                    }
+                    ptx::tc_fence_after_sync();
+                    ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
                 }
                 if (lane == 0) FA_TRACE_EV(warp, g, 0);
                 float mx = -INFINITY;

@@ -1,5 +1,6 @@
-"""Model check of the backward kernel's producer -> issuer named-barrier
-protocol, aborts included (CPU only).
+"""Model check of the kernels' named-barrier protocols, aborts included (CPU
+only): the backward's producer warps -> MMA issuer signals and the forward's
+score issuer -> softmax warps "S ready" signal.
 
 The kernel's roles are replayed as coroutines under random interleavings, with
 the hardware's named-barrier rule: a barrier id counts arriving warps, and
@@ -11,12 +12,12 @@ is a deadlock.  mbarrier waits (the MMA-completion and TMA signals) succeed
 once their event has happened, fail at once after an abort, and may time out
 (raising the abort) at any point before.
 
-Checked: with the kernel's rules -- every signal alternating between two ids
-by generation parity, a producer arriving while healthy and joining with
-bar.sync after an abort, the issuer meeting each producer group's barriers in
-the order that group signals them -- no interleaving overruns or deadlocks,
-whatever waits time out.  The same protocol on a single id per signal does
-overrun, which shows that the check can fail.
+Checked: with the kernels' rules -- a signal that runs P generations ahead
+cycling through P + 1 ids, a producer arriving while healthy and joining
+with bar.sync after an abort, the consumers meeting each producer's barriers
+in the order it signals them -- no interleaving overruns or deadlocks,
+whatever waits time out.  The same protocols with fewer ids do overrun,
+which shows that the check can fail.
 """
 import random
 
@@ -36,7 +37,7 @@ def simulate(roles, expected, seed, p_timeout):
     random schedule.  Yields from a role: ('emit', ev), ('wait', ev) -> bool,
     ('arrive', id), ('sync', id).  Returns whether an abort happened."""
     rng = random.Random(seed)
-    events, bars = set(), {}
+    events, bars, counts = set(), {}, {}
     aborted = False
     state = {n: ("ready", None) for n in roles}
     live = set(roles)
@@ -69,6 +70,11 @@ def simulate(roles, expected, seed, p_timeout):
             continue
         if act[0] == "emit":
             events.add(act[1])
+            state[n] = ("ready", None)
+        elif act[0] == "count":  # one of act[2] arrivals an mbarrier phase needs
+            counts[act[1]] = counts.get(act[1], 0) + 1
+            if counts[act[1]] == act[2]:
+                events.add(act[1])
             state[n] = ("ready", None)
         elif act[0] == "wait":
             state[n] = ("wait", act[1])
@@ -177,6 +183,93 @@ def backward_roles(items, two_ids=True):
     return roles
 
 
+def forward_roles(items, nids=3):
+    """The forward kernel's roles for one CTA walking `items` (key tiles per
+    work item): the TMA producer (its loads assumed to land), the score
+    issuer, the P.V issuer and 8 softmax warps.  Named barriers: S_READY
+    (score issuer -> softmax warps) and the softmax warps' pair barriers;
+    everything else is an mbarrier.  The score stream runs two tiles ahead
+    (S of tile g waits only until S of g - 2 has been read), so a healthy
+    arrival for tile g guarantees only that generation g - 2 has completed:
+    the signal needs three ids."""
+    par = lambda n: n % nids
+
+    def tma():
+        for k in range(len(items)):
+            yield ("emit", ("QFULL", k))
+        for g in range(sum(items)):
+            yield ("emit", ("KFULL", g))
+            yield ("emit", ("VFULL", g))
+
+    def score_issuer():
+        ok, g = True, 0
+
+        def signal(gg):
+            nonlocal ok
+            if ok:
+                ok = yield ("wait", ("SFULL", gg))
+            yield ("arrive" if ok else "sync", ("S_READY", par(gg)))
+
+        for k, n in enumerate(items):
+            for j in range(n):
+                if g >= 1:
+                    yield from signal(g - 1)
+                if j == 0 and ok:
+                    ok = yield ("wait", ("QFULL", k))
+                if ok:
+                    ok = yield ("wait", ("KFULL", g))
+                if g >= 2 and ok:
+                    ok = yield ("wait", ("SREAD", g - 2))
+                if ok:
+                    yield ("emit", ("SFULL", g))
+                g += 1
+        if g >= 1:
+            yield from signal(g - 1)
+
+    def pv_issuer():
+        ok, g = True, 0
+        for k, n in enumerate(items):
+            if ok and k > 0:
+                ok = yield ("wait", ("OFREE", k - 1))
+            for j in range(n):
+                if ok:
+                    ok = yield ("wait", ("VFULL", g))
+                if ok:
+                    ok = yield ("wait", ("PFULL", g))
+                if ok:
+                    yield ("emit", ("ODONE", g))
+                    if j == n - 1:
+                        yield ("emit", ("OFINAL", k))
+                g += 1
+
+    def softmax(w):
+        ok, g = True, 0
+        for k, n in enumerate(items):
+            for j in range(n):
+                yield ("sync", ("S_READY", par(g)))
+                if ok:
+                    yield ("count", ("SREAD", g), 8)
+                yield ("sync", ("PAIR", w % 4))
+                if ok and g >= 1:
+                    ok = yield ("wait", ("ODONE", g - 1))
+                if ok:
+                    yield ("count", ("PFULL", g), 8)
+                g += 1
+            if ok:
+                ok = yield ("wait", ("OFINAL", k))
+            yield ("sync", ("PAIR", w % 4))
+            if ok:
+                yield ("count", ("OFREE", k), 8)
+
+    roles = {"tma": tma(), "score": score_issuer(), "pv": pv_issuer()}
+    roles.update({f"softmax{w}": softmax(w) for w in range(8)})
+    return roles
+
+
+def forward_expected(bid):
+    return 2 if bid[0] == "PAIR" else 9
+
+
 def expected(bid):
     return 9 if bid[0] in ("P_READY", "DP_READ", "DS_READY") else 5  # producer warps + the issuer
 
@@ -203,3 +296,21 @@ def test_single_id_per_signal_overruns_after_an_abort():
         for seed, items, p in cases(600):
             if p > 0:
                 simulate(backward_roles(items, two_ids=False), expected, seed, p)
+
+
+def test_forward_protocol_never_overruns_or_deadlocks():
+    aborted = clean = 0
+    for seed, items, p in cases(600):
+        if simulate(forward_roles(items), forward_expected, seed, p):
+            aborted += 1
+        else:
+            clean += 1
+    assert aborted > 100 and clean > 100
+
+
+@pytest.mark.parametrize("nids", [1, 2])
+def test_forward_fewer_ids_overrun_after_an_abort(nids):
+    with pytest.raises(Overrun):
+        for seed, items, p in cases(600):
+            if p > 0:
+                simulate(forward_roles(items, nids), forward_expected, seed, p)
