@@ -66,18 +66,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "a40a88aed7db209d40a727cbdc6056f3e407fdeed08f4823bf3af9ceea1f9666",
-        "bytes": 4 * (201_396_224 + 44_382_208),
+        "sha256": "fec9ea999744bdb5b07ad457254f5eec625f20d7ad09c78b6a4a2a296b3800a4",
+        "bytes": 4 * (201_397_504 + 44_192_000),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "d26f21087330fe31cae46586f2074eaed399ea0bd2326585770c1ed8eadf0458",
-        "bytes": 4 * (405_911_808 + 217_132_288),
+        "sha256": "9befd60e8da07d559cf223ef5f85c9868f95a2b7dd45526878eb54f368825df9",
+        "bytes": 4 * (406_082_816 + 217_450_240),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "904d3532c0c483d90fe607216f912b7323ac4df26503284682ca281b546f74cc",
-        "bytes": 285_247_488 + 211_092_992,
+        "sha256": "78c9ea833c94112d6fa2b07ccf029de4c5fa03386328393371b155af903ff40e",
+        "bytes": 285_239_296 + 210_451_968,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
