@@ -60,6 +60,19 @@
 // max by more than RESCALE_LOG2 (base-2 units); P, l and l~ share the same
 // reference, so the ratios are unaffected and P stays below 2^RESCALE_LOG2.
 //
+// D = 64 runs a split design (Layout<64>::SPLIT).  Each row is carried as two
+// independent halves h = 0, 1 (keys 64h .. 64h+63 of every tile, the warps w
+// and w+4 of a lane quarter), each with its own reference max m_h, row sum
+// l_h, P written over its half of the S buffer, and accumulator
+// [O_h | l~_h] = sum over tiles of P_h [V_h | 1] (TMEM: S 2 x 128 columns,
+// [O_h | l~_h] 2 x 80).  The halves merge once per item in the epilogue by
+// their maxima, as split-key partial results do: with w_h = 2^(m_h - M),
+// M = max(m_0, m_1), out = (w_0 O_0 + w_1 O_1) / (w_0 l~_0 + w_1 l~_1) and
+// lse = (M + log2(w_0 l_0 + w_1 l_1)) ln 2.  The two warps of a row then never
+// wait for each other inside the tile loop, which pays where the softmax
+// bounds the kernel (d = 64: half the tensor work per tile).  At D = 128 the
+// two [O_h | l~_h] accumulators do not fit next to the S buffers.
+//
 // Head sizes d < D (multiples of 8) run in the D = 64 or 128 instance: the
 // TMA boxes are 64 columns wide and fill columns past d with zeros, which add
 // nothing to any dot product; the epilogue stores d columns with row stride d.
@@ -105,6 +118,10 @@ constexpr uint32_t STATUS_BAD_SMEM = 2u;
 constexpr uint32_t NB_PAIR0 = 1;
 constexpr uint32_t NB_SREADY0 = 5;  // + (g % 3)
 constexpr uint32_t NB_SREADY_COUNT = SOFTMAX_THREADS + 32;
+// The split design (D = 64): one S-ready signal per half-row group, id
+// 5 + 3h + g % 3, met by that group's four warps and the score issuer.
+constexpr uint32_t NB_SREADY_SPLIT0 = 5;
+constexpr uint32_t NB_SREADY_SPLIT_COUNT = SOFTMAX_THREADS / 2 + 32;
 
 // Producer side of a producer -> consumers named barrier; the consumers meet
 // every generation with bar.sync, in order.  While the pipeline runs, the
@@ -142,12 +159,18 @@ struct Params {
 template <int D>
 struct Layout {
     static_assert(D == 64 || D == 128, "head size");
+    // D = 64 runs the split design: the two half-row warps of a row keep
+    // separate softmax states and accumulators [O_h | l~_h] (TMEM has room
+    // for both at D = 64) and merge them in the epilogue.
+    static constexpr bool SPLIT = D == 64;
+    static constexpr uint32_t O_STRIDE = D + 16;  // split design: O_1 follows [O_0 | l~_0]
     static constexpr int KSTAGES = (D == 128) ? 3 : 4;  // K runs two tiles ahead of V
     static constexpr int VSTAGES = (D == 128) ? 2 : 4;
     static constexpr int DBLK = D / 64;                   // 64-column blocks of a row
     static constexpr uint32_t TM_L = TM_O + D;            // l~ columns
     static_assert(TM_L + 16 <= TM_P && TM_P + 64 <= TM_LX && TM_LX + 2 <= TM_MX && TM_MX + 4 <= TM_COLS,
                   "TMEM budget");
+    static_assert(!SPLIT || TM_O + 2 * O_STRIDE <= TM_COLS, "TMEM budget (split)");
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;      // bytes of one K or V tile
     static constexpr uint32_t VSTAGE = (DBLK + 1) * BLK_BYTES;  // V blocks + the ones block
@@ -162,14 +185,17 @@ struct Layout {
     static constexpr int B_VFULL = B_KEMPTY + KSTAGES;
     static constexpr int B_VEMPTY = B_VFULL + VSTAGES;
     static constexpr int B_SFULL = B_VEMPTY + VSTAGES;  // 2 (per S buffer): S written
-    static constexpr int B_SREAD = B_SFULL + 2;         // 2 (per S buffer): S read out
-    static constexpr int B_PFULL = B_SREAD + 2;         // P written
-    static constexpr int B_ODONE = B_PFULL + 1;  // every P.V
-    static constexpr int B_OFINAL = B_ODONE + 1; // the last P.V of an item
+    static constexpr int B_SREAD = B_SFULL + 2;         // 2 (per S buffer): S read out (one-state design)
+    static constexpr int B_PFULL = B_SREAD + 2;         // P written; split: 4 (2 * half + S buffer)
+    static constexpr int B_ODONE = B_PFULL + 4;  // every P.V; split: 2 (per S buffer, both halves)
+    static constexpr int B_OFINAL = B_ODONE + 2; // the last P.V of an item
     static constexpr int B_OFREE = B_OFINAL + 1;
     static constexpr int B_DRAIN = B_OFREE + 1;  // 2 (one per MMA issuer)
     static constexpr int NUM_BARS = B_DRAIN + 2;
-    static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;  // [0] TMEM base, [1] abort
+    // Split design: the epilogue's (m, l, l~) exchange, one slot per item parity.
+    static constexpr uint32_t OFF_XCH = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
+    static constexpr uint32_t XCH_BYTES = SPLIT ? 2 * 6 * BM * 4 : 0;
+    static constexpr uint32_t OFF_MISC = OFF_XCH + XCH_BYTES;  // [0] TMEM base, [1] abort
     // The dynamic shared memory base is 1024-byte aligned (no static shared
     // memory); the kernel checks it and refuses to run otherwise.
     static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
@@ -289,6 +315,22 @@ __device__ __forceinline__ void scale_cols(uint32_t taddr, float corr)
     }
 }
 
+// Multiplies this thread's D columns of an O accumulator (TMEM, from `taddr`)
+// by `corr` (the split design).
+template <int D>
+__device__ __forceinline__ void scale_row(uint32_t taddr, float corr)
+{
+#pragma unroll
+    for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t o[32];
+        ptx::tmem_ld32(taddr + ch * 32, o);
+        ptx::tmem_wait_ld(o);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * corr);
+        ptx::tmem_st32(taddr + ch * 32, o);
+    }
+}
+
 // Work item i: (flattened head, query block).  Within a head the blocks come
 // heavy, light, heavy, light (m = M-1, 0, M-2, 1, ...), and a CTA always takes
 // the two items of a pair (2p, 2p+1): under the causal mask every pair then
@@ -359,10 +401,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Softmax-side barriers count warps: each warp arrives once, after __syncwarp.
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(L::B_SFULL + b), 1);
-            ptx::mbar_init(bar(L::B_SREAD + b), SOFTMAX_WARPS);
+            if constexpr (L::SPLIT) {
+                ptx::mbar_init(bar(L::B_PFULL + b), SOFTMAX_WARPS / 2);
+                ptx::mbar_init(bar(L::B_PFULL + 2 + b), SOFTMAX_WARPS / 2);
+                ptx::mbar_init(bar(L::B_ODONE + b), 1);
+            } else {
+                ptx::mbar_init(bar(L::B_SREAD + b), SOFTMAX_WARPS);
+            }
         }
-        ptx::mbar_init(bar(L::B_PFULL), SOFTMAX_WARPS);
-        ptx::mbar_init(bar(L::B_ODONE), 1);
+        if constexpr (!L::SPLIT) {
+            ptx::mbar_init(bar(L::B_PFULL), SOFTMAX_WARPS);
+            ptx::mbar_init(bar(L::B_ODONE), 1);
+        }
         ptx::mbar_init(bar(L::B_OFINAL), 1);
         ptx::mbar_init(bar(L::B_OFREE), SOFTMAX_WARPS);
         ptx::mbar_init(bar(L::B_DRAIN), 1);
@@ -503,7 +553,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                        0x200 + L::B_SFULL + (gg & 1));
             ptx::tc_fence_before_sync();
             __syncwarp();
-            nb_signal(NB_SREADY0 + (uint32_t)(gg % 3), NB_SREADY_COUNT, ok);
+            if constexpr (L::SPLIT) {
+                nb_signal(NB_SREADY_SPLIT0 + (uint32_t)(gg % 3), NB_SREADY_SPLIT_COUNT, ok);       // half 0
+                nb_signal(NB_SREADY_SPLIT0 + 3u + (uint32_t)(gg % 3), NB_SREADY_SPLIT_COUNT, ok);  // half 1
+            } else {
+                nb_signal(NB_SREADY0 + (uint32_t)(gg % 3), NB_SREADY_COUNT, ok);
+            }
         };
         for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step), ++k) {
             const int n = item_of<CAUSAL>(i, p).n_kv;
@@ -520,8 +575,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // Buffer b is free once every softmax warp has read S of tile
                 // g - 2 (the phase before cannot alias: S of g - 2 was issued
                 // only after S of g - 4 had been read).
-                if (g >= 2 && ok) ok = warp_wait_bar(bar(L::B_SREAD + b), (uint32_t)((g - 2) >> 1) & 1u, limit,
-                                                     abort_flag, 0x200 + L::B_SREAD + b);
+                // Split design: P of tile g - 2 lies over its scores, so buffer
+                // b is free once both halves' P.V of g - 2 are complete.
+                if (g >= 2 && ok) {
+                    const int bb = L::SPLIT ? L::B_ODONE + b : L::B_SREAD + b;
+                    ok = warp_wait_bar(bar(bb), (uint32_t)((g - 2) >> 1) & 1u, limit, abort_flag, 0x200 + bb);
+                }
                 if (!ok) continue;
                 if (lane == 0) FA_TRACE_EV(9, g, 0);
                 ptx::tc_fence_after_sync();
@@ -552,6 +611,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // per column, 8 columns per 16 keys); B MN-major (value columns
         // contiguous): 64-column blocks BLK_BYTES apart (the ones block follows
         // the value blocks), 8-key groups 1024 bytes apart.
+        if constexpr (L::SPLIT) {
+        // [O_h | l~_h] (+)= P_h [V_h | 1] for global tile g and each half h:
+        // A = P_h from TMEM (over the half's scores in S buffer g & 1; 2 bf16
+        // per column, 8 columns per 16 keys), B = value rows 64h .. 64h+63,
+        // MN-major (value columns contiguous): 64-column blocks BLK_BYTES
+        // apart (the ones block follows the value blocks), 8-key groups 1024
+        // bytes apart.  Each half's P is taken as soon as it is written.
+        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
+        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
+        int g = 0, k = 0;  // tiles and items done
+        bool ok = true;
+        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+            const int n = item_of<CAUSAL>(i, p).n_kv;
+            // The first P.V of an item overwrites O: wait until the softmax
+            // warps have read out the previous item's O.
+            if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                     0x200 + L::B_OFREE)))
+                break;
+            for (int j = 0; ok && j < n; ++j, ++g) {
+                const int s = g % L::VSTAGES;
+                const int b = g & 1;
+                // V of tile g, loaded long before, is checked first: an mbarrier
+                // check is slow while the score MMAs stream their operands, and
+                // it then overlaps the softmax warps' work on P.
+                if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
+                                         abort_flag, 0x200 + L::B_VFULL + s)))
+                    break;
+                if (lane == 0) FA_TRACE_EV(10, g, 3);
+                const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
+                const uint32_t s_tm = tmem + (b ? TM_S1 : TM_S0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // P_h of tile g (per S buffer: the phase before, tile g - 2,
+                    // was consumed by this warp, so parity cannot alias).
+                    if (!(ok = warp_wait_bar(bar(L::B_PFULL + 2 * h + b), (uint32_t)(g >> 1) & 1u, limit,
+                                             abort_flag, 0x200 + L::B_PFULL + 2 * h + b)))
+                        break;
+                    ptx::tc_fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (ptx::elect_one())
+                            ptx::mma_ts(tmem + TM_O + (uint32_t)h * L::O_STRIDE, s_tm + (uint32_t)(h * 64 + kk * 8),
+                                        v_desc + (uint64_t)(((h * 64 + kk * 16) * 128) >> 4), IDESC_O,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                if (ptx::elect_one()) {
+                    // The commits cover every MMA this warp issued so far.
+                    ptx::tc_commit(bar(L::B_VEMPTY + s));
+                    ptx::tc_commit(bar(L::B_ODONE + b));
+                    if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
+                    FA_TRACE_EV(10, g, 4);
+                }
+            }
+        }
+        } else {
         constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
         const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
         const uint32_t p_tmem = tmem + TM_P;
@@ -598,9 +714,202 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        }
         if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN + 1));
         drain_bar(bar(L::B_DRAIN + 1), 0, limit, abort_flag, 0x281);
     } else {
+      if constexpr (L::SPLIT) {
+        // ------------------------------------- softmax warps, split design
+        // Warp w serves query rows 32*(w%4) .. +31 (its TMEM lane quarter) and
+        // score columns 64*h .. +63, h = w/4, with a state of its own: its
+        // reference max, its row sum, its P (written over its half of the S
+        // buffer) and its accumulator [O_h | l~_h] = sum over tiles of
+        // P_h [V_h | 1].  The two halves of a row meet once per item, in the
+        // epilogue.
+        const int quarter = warp & 3;
+        const int half = warp >> 2;
+        const int row = quarter * 32 + lane;      // query row in the item == TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t o_mine = tmem + lane_off + TM_O + (uint32_t)half * L::O_STRIDE;
+        const float sl2 = p.scale_log2;
+        const uint32_t nb_sready = NB_SREADY_SPLIT0 + 3u * (uint32_t)half;
+        float* const xch = reinterpret_cast<float*>(sgen + L::OFF_XCH);
+        bool ok = true;
+        int g = 0;      // tiles done
+        int kitem = 0;  // items done
+
+        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
+            const Item it = item_of<CAUSAL>(i, p);
+            const int q_idx = it.q0 + row;
+            const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
+            const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
+            float m_ref = -INFINITY;
+            // This half-row's sum of probabilities, as four packed fp32 pairs.
+            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+            {
+            // This half-row's scores (fp32 bit patterns), used in place: the
+            // packed fp32x2 arithmetic takes neighbouring load registers as
+            // its operand pairs.
+            uint32_t sr[64];
+
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const int b = g & 1;
+                const uint32_t s_half = tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64;
+                // S of tile g is in TMEM (met on every tile, also after an abort).
+                ptx::named_barrier_sync(nb_sready + (uint32_t)(g % 3), NB_SREADY_SPLIT_COUNT);
+                if (!ok) continue;
+                ptx::tc_fence_after_sync();
+                ptx::tmem_ld64(s_half, sr);
+                if (lane == 0) FA_TRACE_EV(warp, g, 0);
+                ptx::tmem_wait_ld64(sr);
+                if (lane == 0) FA_TRACE_EV(warp, g, 1);
+                // Causal diagonal tile / keys past N: -inf before the max.
+                const int k0 = j * BN + half * 64;
+                if (j * BN + BN - 1 > cta_key_max) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
+                }
+                const float m_tile = max64(sr) * sl2;  // scale > 0, so max commutes with it
+                if (lane == 0) FA_TRACE_EV(warp, g, 2);
+
+                // A half-row may have no visible key yet (its reference then
+                // stays -inf and its P, O_h and l are 0).
+                if (j == 0) {
+                    m_ref = m_tile;
+                } else {
+                    const float m_new = fmaxf(m_ref, m_tile);
+                    const bool need = m_new > m_ref + RESCALE_LOG2;
+                    if (__any_sync(0xffffffffu, need)) {
+                        // O_h holds everything up to the previous tile once
+                        // both halves' P.V of it are done (the phase before,
+                        // tile g - 3, cannot alias: tile g - 1 was issued only
+                        // after it).
+                        if (!(ok = warp_wait_bar(bar(L::B_ODONE + ((g - 1) & 1)), (uint32_t)((g - 1) >> 1) & 1u,
+                                                 limit, abort_flag, 0x300 + L::B_ODONE + ((g - 1) & 1))))
+                            continue;
+                        ptx::tc_fence_after_sync();
+                        const float corr = ptx::ex2(m_ref - m_new);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
+
+                        m_ref = m_new;
+                        scale_row<D>(o_mine, corr);
+                        uint32_t lt[8];
+                        ptx::tmem_ld8(o_mine + D, lt);
+                        ptx::tmem_wait_ld_only();
+                        ptx::reg_fence8(lt);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) lt[c] = __float_as_uint(__uint_as_float(lt[c]) * corr);
+                        ptx::tmem_st8(o_mine + D, lt);
+                        ptx::tmem_wait_st();
+                    }
+                }
+
+                // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
+                // scaling and the sums use packed fp32x2 instructions: fewer
+                // issue slots, which the MMA issuers on the same sub-partitions
+                // need.
+                const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                const uint64_t neg_m2 = ptx::f2_pack(-m_use, -m_use);
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float x0, x1;
+                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                               sl2x2, neg_m2),
+                                   x0, x1);
+                    const float a0 = ptx::ex2(x0);
+                    const float a1 = ptx::ex2(x1);
+                    lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
+                    pk[c] = ptx::pack_bf16x2(a0, a1);
+                }
+                if (lane == 0) FA_TRACE_EV(warp, g, 3);
+
+                // P over this half's scores (read into registers above).
+                ptx::tmem_st32(s_half, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + 2 * half + b));
+                if (lane == 0) FA_TRACE_EV(warp, g, 5);
+            }
+            }
+
+            // --------------------------------------------------- epilogue
+            // With w_h = 2^(m_h - M), M = max(m_0, m_1):
+            //   O   = (w_0 O_0 + w_1 O_1) / (w_0 l~_0 + w_1 l~_1)   (l~: sums of the rounded P)
+            //   lse = (M + log2(w_0 l_0 + w_1 l_1)) ln 2            (l: sums of the fp32 P)
+            // The two halves' (m, l, l~) meet through shared memory (one
+            // slot per item parity, so the next item's write never meets this
+            // item's read).
+            if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
+                                       0x380 + L::B_OFINAL);
+            float l_lo, l_hi;
+            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
+            const float l_mine = l_lo + l_hi;
+            float lr_mine = 0.f;
+            if (ok) {
+                ptx::tc_fence_after_sync();
+                uint32_t lt[8];
+                ptx::tmem_ld8(o_mine + D, lt);
+                ptx::tmem_wait_ld_only();
+                ptx::reg_fence8(lt);
+                lr_mine = __uint_as_float(lt[0]);
+            }
+            float* const slot = xch + (kitem & 1) * (6 * BM);
+            slot[(3 * half) * BM + row] = m_ref;
+            slot[(3 * half + 1) * BM + row] = l_mine;
+            slot[(3 * half + 2) * BM + row] = lr_mine;
+            ++kitem;
+            ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
+            if (ok) {
+                const float m_other = slot[(3 * (half ^ 1)) * BM + row];
+                const float l_other = slot[(3 * (half ^ 1) + 1) * BM + row];
+                const float lr_other = slot[(3 * (half ^ 1) + 2) * BM + row];
+                const float m_max = fmaxf(m_ref, m_other);
+                const float s_mine = ptx::ex2(m_ref - m_max);
+                const float s_other = ptx::ex2(m_other - m_max);
+                const float l = l_mine * s_mine + l_other * s_other;
+                const float inv_l = 1.0f / (lr_mine * s_mine + lr_other * s_other);
+                const float s0 = (half == 0 ? s_mine : s_other) * inv_l;
+                const float s1 = (half == 0 ? s_other : s_mine) * inv_l;
+                const bool row_ok = q_idx < N;
+                // A head size d below D was zero-padded by the TMA loads: the
+                // padded columns of O are zero and not stored.
+                __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
+                const uint32_t o0 = tmem + lane_off + TM_O + (uint32_t)half * (D / 2);
+#pragma unroll
+                for (int ch = 0; ch < D / 64; ++ch) {
+                    uint32_t oa[32], ob[32];
+                    ptx::tmem_ld32(o0 + ch * 32, oa);
+                    ptx::tmem_ld32(o0 + L::O_STRIDE + ch * 32, ob);
+                    ptx::tmem_wait_ld(oa);
+                    ptx::reg_fence(ob);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        w[c] = ptx::pack_bf16x2(
+                            fmaf(__uint_as_float(oa[2 * c]), s0, __uint_as_float(ob[2 * c]) * s1),
+                            fmaf(__uint_as_float(oa[2 * c + 1]), s0, __uint_as_float(ob[2 * c + 1]) * s1));
+                    if (row_ok) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
+                                ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                  w[4 * u + 3]);
+                    }
+                }
+                if (half == 0 && row_ok)
+                    p.lse[(int64_t)it.bh * N + q_idx] = (m_max + ptx::lg2(l)) * 0.69314718055994530942f;
+                // O has been read: the next item's first P.V may overwrite it.
+                ptx::tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
+            }
+        }
+      } else {
         // ---------------------------------------------------- softmax warps
         const int quarter = warp & 3;
         const int half = warp >> 2;               // score columns [64*half, 64*half+64)
@@ -802,6 +1111,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
             }
         }
+      }
     }
 
     ptx::tc_fence_before_sync();

@@ -270,6 +270,91 @@ def forward_expected(bid):
     return 2 if bid[0] == "PAIR" else 9
 
 
+def forward_split_roles(items, nids=3):
+    """The forward kernel's roles at D = 64 (the split design): the two
+    half-row groups of softmax warps keep separate states, each with its own
+    S_READY signal from the score issuer (4 warps + the issuer), per-buffer
+    P-written barriers, and a score issuer that reuses an S buffer once both
+    halves' P.V of the tile two back are done; the halves meet in the
+    epilogue's pair barriers."""
+    par = lambda n: n % nids
+
+    def tma():
+        for k in range(len(items)):
+            yield ("emit", ("QFULL", k))
+        for g in range(sum(items)):
+            yield ("emit", ("KFULL", g))
+            yield ("emit", ("VFULL", g))
+
+    def score_issuer():
+        ok, g = True, 0
+
+        def signal(gg):
+            nonlocal ok
+            if ok:
+                ok = yield ("wait", ("SFULL", gg))
+            for h in (0, 1):
+                yield ("arrive" if ok else "sync", ("S_READY", h, par(gg)))
+
+        for k, n in enumerate(items):
+            for j in range(n):
+                if g >= 1:
+                    yield from signal(g - 1)
+                if j == 0 and ok:
+                    ok = yield ("wait", ("QFULL", k))
+                if ok:
+                    ok = yield ("wait", ("KFULL", g))
+                if g >= 2 and ok:
+                    ok = yield ("wait", ("ODONE", g - 2))
+                if ok:
+                    yield ("emit", ("SFULL", g))
+                g += 1
+        if g >= 1:
+            yield from signal(g - 1)
+
+    def pv_issuer():
+        ok, g = True, 0
+        for k, n in enumerate(items):
+            if ok and k > 0:
+                ok = yield ("wait", ("OFREE", k - 1))
+            for j in range(n):
+                if ok:
+                    ok = yield ("wait", ("VFULL", g))
+                for h in (0, 1):
+                    if ok:
+                        ok = yield ("wait", ("PFULL", h, g))
+                if ok:
+                    yield ("emit", ("ODONE", g))
+                    if j == n - 1:
+                        yield ("emit", ("OFINAL", k))
+                g += 1
+
+    def softmax(w):
+        h = w // 4
+        ok, g = True, 0
+        for k, n in enumerate(items):
+            for j in range(n):
+                yield ("sync", ("S_READY", h, par(g)))
+                if ok and j > 0 and g % 5 == 3:  # a rescale now and then waits for P.V of g - 1
+                    ok = yield ("wait", ("ODONE", g - 1))
+                if ok:
+                    yield ("count", ("PFULL", h, g), 4)
+                g += 1
+            if ok:
+                ok = yield ("wait", ("OFINAL", k))
+            yield ("sync", ("PAIR", w % 4))
+            if ok:
+                yield ("count", ("OFREE", k), 8)
+
+    roles = {"tma": tma(), "score": score_issuer(), "pv": pv_issuer()}
+    roles.update({f"softmax{w}": softmax(w) for w in range(8)})
+    return roles
+
+
+def forward_split_expected(bid):
+    return 2 if bid[0] == "PAIR" else 5
+
+
 def expected(bid):
     return 9 if bid[0] in ("P_READY", "DP_READ", "DS_READY") else 5  # producer warps + the issuer
 
@@ -314,3 +399,20 @@ def test_forward_fewer_ids_overrun_after_an_abort(nids):
         for seed, items, p in cases(600):
             if p > 0:
                 simulate(forward_roles(items, nids), forward_expected, seed, p)
+
+
+def test_forward_split_protocol_never_overruns_or_deadlocks():
+    aborted = clean = 0
+    for seed, items, p in cases(600):
+        if simulate(forward_split_roles(items), forward_split_expected, seed, p):
+            aborted += 1
+        else:
+            clean += 1
+    assert aborted > 100 and clean > 100
+
+
+def test_forward_split_two_ids_overrun_after_an_abort():
+    with pytest.raises(Overrun):
+        for seed, items, p in cases(600):
+            if p > 0:
+                simulate(forward_split_roles(items, 2), forward_split_expected, seed, p)
