@@ -89,27 +89,38 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 }
 
 // Per-device, per-kernel one-time set-up (opt-in shared memory size).
-template <int D, bool CAUSAL, bool PAD>
+template <int D, bool CAUSAL, bool PAD, bool SNAKE>
 cudaError_t prepare_kernel(int dev)
 {
     static std::atomic<int> done[MAX_DEVICES];
     if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
     if (done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, PAD>,
+    cudaError_t e = cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, PAD, SNAKE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)fa::Layout<D>::SMEM_BYTES);
     if (e == cudaSuccess) done[dev].store(1, std::memory_order_release);
     return e;
 }
 
-template <int D, bool CAUSAL, bool PAD = false>
-fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                 const fa::Params& p, unsigned grid, int dev, cudaStream_t stream)
+template <int D, bool CAUSAL, bool PAD, bool SNAKE>
+fa_status launch_one(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                     const fa::Params& p, unsigned grid, int dev, cudaStream_t stream)
 {
-    if (prepare_kernel<D, CAUSAL, PAD>(dev) != cudaSuccess) return FA_ERR_CUDA;
-    fa::fa_fwd_kernel<D, CAUSAL, PAD>
+    if (prepare_kernel<D, CAUSAL, PAD, SNAKE>(dev) != cudaSuccess) return FA_ERR_CUDA;
+    fa::fa_fwd_kernel<D, CAUSAL, PAD, SNAKE>
         <<<grid, fa::NUM_THREADS, fa::Layout<D>::SMEM_BYTES, stream>>>(mq, mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Causal problems run in cost order (snake) when `snake`; see item_of.
+template <int D, bool CAUSAL, bool PAD = false>
+fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                 const fa::Params& p, unsigned grid, int dev, cudaStream_t stream, bool snake)
+{
+    if constexpr (CAUSAL) {
+        if (snake) return launch_one<D, true, PAD, true>(mq, mk, mv, p, grid, dev, stream);
+    }
+    return launch_one<D, CAUSAL, PAD, false>(mq, mk, mv, p, grid, dev, stream);
 }
 
 // Number of SMs of a device (cached): the kernel is persistent, one CTA per SM.
@@ -422,25 +433,33 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.N = (int)N;
     p.d = (int)d;
     p.num_m_blocks = (int)m_blocks;
+    p.num_bh = (int)BH;
     p.num_items = (int)(BH * m_blocks);
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     p.debug_skip_k = g_debug_skip_k.load(std::memory_order_relaxed);
-    // One CTA per SM, at most one per pair of work items.
-    const unsigned grid = (unsigned)std::min<int64_t>((BH * m_blocks + 1) / 2, sms);
+    // Causal items differ in cost.  Heavy/light pairs of a head keep its K/V
+    // in L2 while its blocks run; when all heads' K and V fit in L2 anyway,
+    // ordering the items by cost balances the CTAs better (see item_of).
+    int l2_bytes = 0;
+    if (cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return FA_ERR_CUDA;
+    const double kv_bytes = 2.0 * (double)BH * (double)N * (double)d * 2.0;
+    const bool snake = causal && kv_bytes <= 0.6 * (double)l2_bytes;
+    // One CTA per SM, at most one per work item (per pair of items in pair order).
+    const unsigned grid = (unsigned)std::min<int64_t>(snake ? BH * m_blocks : (BH * m_blocks + 1) / 2, sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     if (d == 128)
-        return causal ? launch<128, true>(mq, mk, mv, p, grid, dev, st)
-                      : launch<128, false>(mq, mk, mv, p, grid, dev, st);
+        return causal ? launch<128, true>(mq, mk, mv, p, grid, dev, st, snake)
+                      : launch<128, false>(mq, mk, mv, p, grid, dev, st, snake);
     if (d == 64)
-        return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st)
-                      : launch<64, false>(mq, mk, mv, p, grid, dev, st);
+        return causal ? launch<64, true>(mq, mk, mv, p, grid, dev, st, snake)
+                      : launch<64, false>(mq, mk, mv, p, grid, dev, st, snake);
     if (d > 64)
-        return causal ? launch<128, true, true>(mq, mk, mv, p, grid, dev, st)
-                      : launch<128, false, true>(mq, mk, mv, p, grid, dev, st);
-    return causal ? launch<64, true, true>(mq, mk, mv, p, grid, dev, st)
-                  : launch<64, false, true>(mq, mk, mv, p, grid, dev, st);
+        return causal ? launch<128, true, true>(mq, mk, mv, p, grid, dev, st, snake)
+                      : launch<128, false, true>(mq, mk, mv, p, grid, dev, st, snake);
+    return causal ? launch<64, true, true>(mq, mk, mv, p, grid, dev, st, snake)
+                  : launch<64, false, true>(mq, mk, mv, p, grid, dev, st, snake);
 }
 
 fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, size_t* bytes)

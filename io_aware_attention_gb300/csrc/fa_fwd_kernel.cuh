@@ -150,6 +150,7 @@ struct Params {
     int N;
     int d;  // the caller's head size (<= D, a multiple of 8): O's row stride and stored columns
     int num_m_blocks;
+    int num_bh;        // B * H
     int num_items;
     float scale_log2;  // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -331,13 +332,34 @@ __device__ __forceinline__ void scale_row(uint32_t taddr, float corr)
     }
 }
 
-// Work item i: (flattened head, query block).  Within a head the blocks come
-// heavy, light, heavy, light (m = M-1, 0, M-2, 1, ...), and a CTA always takes
-// the two items of a pair (2p, 2p+1): under the causal mask every pair then
-// costs the same M + 1 key tiles, which balances the static schedule.
+// Work item i: (flattened head, query block).  Two static orders:
+//  - pairs (SNAKE == false): within a head the blocks come heavy, light, heavy,
+//    light (m = M-1, 0, M-2, 1, ...), and a CTA always takes the two items of
+//    a pair (2p, 2p+1): under the causal mask every pair then costs the same
+//    M + 1 key tiles, and a head's blocks run at the same time on
+//    neighbouring SMs, so its K/V are read from L2;
+//  - by cost (SNAKE, causal problems whose K and V fit in L2): item
+//    rank r is query block M - 1 - r / BH of head r % BH (heaviest first), and
+//    CTA c takes ranks c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (G CTAs): with
+//    fewer pairs than a few per CTA, this balances far better.  A rank is
+//    turned into the item's index in the pair order (item_of_rank), so that
+//    item_of serves both.
 struct Item {
     int bh, q0, n_kv;
 };
+
+// Index (in the pair order) of the item of cost rank r; num_items once the
+// ranks are exhausted.
+__device__ __forceinline__ int item_of_rank(int r, const Params& p)
+{
+    if (r >= p.num_items) return p.num_items;
+    const int M = p.num_m_blocks;
+    const int level = r / p.num_bh;
+    const int bh = r - level * p.num_bh;
+    const int m = M - 1 - level;
+    const int t = (2 * (M - 1 - m) < M) ? 2 * (M - 1 - m) : 2 * m + 1;
+    return bh * M + t;
+}
 
 template <bool CAUSAL>
 __device__ __forceinline__ Item item_of(int i, const Params& p)
@@ -353,8 +375,9 @@ __device__ __forceinline__ Item item_of(int i, const Params& p)
 }
 
 // PAD: the caller's head size p.d is below D (stores are guarded and strided
-// by p.d); the instances for d = D compile without the guard.
-template <int D, bool CAUSAL, bool PAD>
+// by p.d); the instances for d = D compile without the guard.  SNAKE: the
+// items run in cost order (see item_of).
+template <int D, bool CAUSAL, bool PAD, bool SNAKE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p)
@@ -375,11 +398,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint64_t limit = p.wait_limit_ns;
     const int N = p.N;
-    // This CTA's items: pairs p = blockIdx.x, blockIdx.x + gridDim.x, ...,
-    // both items 2p and 2p + 1 of each pair.
-    auto first_item = [&]() -> int { return 2 * (int)blockIdx.x; };
+    // This CTA's items (see item_of): pairs p = blockIdx.x, blockIdx.x +
+    // gridDim.x, ..., both items 2p and 2p + 1 of each pair; or ranks in snake
+    // order.
+    auto first_item = [&]() -> int {
+        return SNAKE ? item_of_rank((int)blockIdx.x, p) : 2 * (int)blockIdx.x;
+    };
     auto next_item = [&](int i, int& step) -> int {
         ++step;
+        if constexpr (SNAKE) {
+            const int G = (int)gridDim.x;
+            return item_of_rank(step * G + ((step & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x), p);
+        }
         return (step & 1) ? i + 1 : i - 1 + 2 * (int)gridDim.x;
     };
 #ifdef FA_TRACE
