@@ -66,18 +66,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "fec9ea999744bdb5b07ad457254f5eec625f20d7ad09c78b6a4a2a296b3800a4",
-        "bytes": 4 * (201_397_504 + 44_192_000),
+        "sha256": "51b9d5ae2f55b828c5b6d04292b0aa19ab8f9e2a2e061913b67f438cb5861313",
+        "bytes": 4 * (201_396_736 + 44_611_328),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "9befd60e8da07d559cf223ef5f85c9868f95a2b7dd45526878eb54f368825df9",
-        "bytes": 4 * (406_082_816 + 217_450_240),
+        "sha256": "f5d465d898bb4ab7e02fe8ae935a7664e6f50e897d48619f494f2d41e113a366",
+        "bytes": 4 * (406_162_432 + 217_304_320),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "78c9ea833c94112d6fa2b07ccf029de4c5fa03386328393371b155af903ff40e",
-        "bytes": 285_239_296 + 210_451_968,
+        "sha256": "4555719982ca73e5e9858fa100bf10c3818f7169290012aa2bcc0d36d2bdc9bd",
+        "bytes": 285_265_408 + 210_365_952,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
