@@ -14,7 +14,10 @@ causal mask.
   extra flush is made between launches.
 * e2e: the same metric through the public call with host buffers: every step
   copies Q, K, V from pinned host memory to the device, runs fa_fwd and copies
-  O and the logsumexp back.
+  O and the logsumexp back, all inside the timed region.  As in a serving
+  loop, the copies in, the compute and the copies out run on three streams
+  with two device buffer sets, so one step's copies overlap its neighbours'
+  compute (pipelined_e2e).
 * roofline: the attention kernel is tensor-core bound; achieved = algorithmic
   FLOPs per launch / mean launch time, against the measured bf16 GEMM peak.
 * cpu_baseline: the fp64 CPU oracle timed on the host cores over a bounded
@@ -144,6 +147,88 @@ def job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
     """Whole-job throughput: every rank runs its own copy of the workload (weak
     scaling), timed by the slowest rank."""
     return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
+def pipelined_e2e(n_steps, host_in, out_like, compute, nbuf=2, lanes=1):
+    """Milliseconds per step of n_steps end-to-end steps.  A step copies the
+    pinned host tensors `host_in` to the device, runs `compute(ins, outs,
+    stream)` (the public call, writing the device tensors `outs`) and copies
+    `outs` back to pinned host tensors.  nbuf sets of device buffers; the
+    copies in, the compute and the copies out run on separate streams linked
+    by events, so that the next step's copies in and the previous step's
+    copies out run while a step computes, as a serving loop would.  With
+    lanes > 1 each direction's copies are cut into pieces spread over that
+    many streams (measured slower for the attention steps: one stream per
+    direction is the default).  Every copy of every step
+    lies inside the timed region (CUDA events from before the first copy in
+    to after the last copy out)."""
+    import torch
+
+    dev_in = [[torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in host_in] for _ in range(nbuf)]
+    dev_out = [[torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in out_like] for _ in range(nbuf)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out_like] for _ in range(nbuf)]
+    s_in = [torch.cuda.Stream() for _ in range(lanes)]
+    s_out = [torch.cuda.Stream() for _ in range(lanes)]
+    s_comp = torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(lanes)] for _ in range(nbuf)]
+    ev_comp = [torch.cuda.Event() for _ in range(nbuf)]
+    ev_out = [[torch.cuda.Event() for _ in range(lanes)] for _ in range(nbuf)]
+
+    def pieces(dsts, srcs):
+        # (dst, src) views of about equal size, `lanes` per tensor
+        out = []
+        for d, h in zip(dsts, srcs):
+            dv, hv = d.view(-1), h.view(-1)
+            n = dv.numel()
+            step = -(-n // lanes)
+            out += [(dv[i:i + step], hv[i:i + step]) for i in range(0, n, step)]
+        return out
+
+    plan_in = [pieces(dev_in[b], host_in) for b in range(nbuf)]
+    plan_out = [pieces(host_out[b], dev_out[b]) for b in range(nbuf)]
+
+    def run(n):
+        for i in range(n):
+            b = i % nbuf
+            for j, s in enumerate(s_in):
+                if i >= nbuf:
+                    s.wait_event(ev_comp[b])  # the step that last used buffer set b has read its inputs
+                with torch.cuda.stream(s):
+                    for d, h in plan_in[b][j::lanes]:
+                        d.copy_(h, non_blocking=True)
+                ev_in[b][j].record(s)
+                s_comp.wait_event(ev_in[b][j])
+            if i >= nbuf:
+                for e in ev_out[b]:
+                    s_comp.wait_event(e)  # ... and its outputs have been copied out
+            compute(dev_in[b], dev_out[b], s_comp)
+            ev_comp[b].record(s_comp)
+            for j, s in enumerate(s_out):
+                s.wait_event(ev_comp[b])
+                with torch.cuda.stream(s):
+                    for h, d in plan_out[b][j::lanes]:
+                        h.copy_(d, non_blocking=True)
+                ev_out[b][j].record(s)
+
+    run(nbuf + 1)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    start.record(s_comp)
+    for s in s_in:
+        s.wait_event(start)
+    run(n_steps)
+    end = torch.cuda.Event(enable_timing=True)
+    for e in ev_out[(n_steps - 1) % nbuf]:
+        s_comp.wait_event(e)
+    for b in range(nbuf):
+        for e in ev_out[b]:
+            s_comp.wait_event(e)
+    end.record(s_comp)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / n_steps
+
+
+E2E_OVERLAP = "copies in / compute / copies out on three streams, two device buffer sets"
 
 
 def dist_env():
@@ -367,31 +452,18 @@ def run_decode(args, w, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-        op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        host_in = [t.pin_memory() for t in (q_h, k_h, v_h)]
         n_e2e = max(3, min(args.steps, 5))
 
-        def e2e_step():
-            q.copy_(qp, non_blocking=True)
-            k.copy_(kp, non_blocking=True)
-            v.copy_(vp, non_blocking=True)
-            fa.decode_into(q, k, v, o, lse, ws, w.causal, w.scale)
-            op.copy_(o, non_blocking=True)
-            lp.copy_(lse, non_blocking=True)
+        # The workspace is shared: every compute runs on the one compute stream.
+        def decode_step(ins, outs, s):
+            fa.decode_into(*ins, *outs, ws, w.causal, w.scale, stream=s)
 
-        e2e_step()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = max_over_ranks(e0.elapsed_time(e1), dev)
-        e2e = {"value": nbytes * world / (ems / n_e2e * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems / n_e2e,
+        ems = max_over_ranks(pipelined_e2e(n_e2e, host_in, (o, lse), decode_step), dev)
+        e2e = {"value": nbytes * world / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems,
                "steps": n_e2e, "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (q, k, v)),
-               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()}
+               "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size(),
+               "overlap": E2E_OVERLAP}
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["hbm_gbs"])
@@ -527,32 +599,19 @@ def run_bwd(args, w, config, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        pinned = [t.pin_memory() for t in (q_h, k_h, v_h, do_h)]
-        op, lp = o.cpu().pin_memory(), lse.cpu().pin_memory()
-        outs = [torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3)]
-
-        def e2e_step():
-            for dst, src in zip((q, k, v, do), pinned):
-                dst.copy_(src, non_blocking=True)
-            o.copy_(op, non_blocking=True)
-            lse.copy_(lp, non_blocking=True)
-            step()
-            for dst, src in zip(outs, (dq, dk, dv)):
-                dst.copy_(src, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize()
+        host_in = [t.pin_memory() for t in (q_h, k_h, v_h)] + [o.cpu().pin_memory(), lse.cpu().pin_memory(),
+                                                              do_h.pin_memory()]
         n_e2e = max(3, min(args.steps, 10))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = max_over_ranks(e0.elapsed_time(e1), dev)
+
+        # The workspace is shared: every compute runs on the one compute stream.
+        def bwd_step(ins, outs, s):
+            fa.bwd_into(*ins, *outs, ws, w.causal, w.scale, stream=s)
+
+        ems = max_over_ranks(pipelined_e2e(n_e2e, host_in, (dq, dk, dv), bwd_step), dev)
         tb = q.numel() * q.element_size()
-        e2e = {"value": job_tflops(flops, world, ems / n_e2e), "unit": "TFLOP/s", "ms_per_step": ems / n_e2e,
-               "steps": n_e2e, "h2d_bytes_per_step": 5 * tb + lse.numel() * 4, "d2h_bytes_per_step": 3 * tb}
+        e2e = {"value": job_tflops(flops, world, ems), "unit": "TFLOP/s", "ms_per_step": ems,
+               "steps": n_e2e, "h2d_bytes_per_step": 5 * tb + lse.numel() * 4, "d2h_bytes_per_step": 3 * tb,
+               "overlap": E2E_OVERLAP}
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
@@ -681,29 +740,16 @@ def run_ew(args, w, rank, world, local):
 
     e2e = None
     if not args.no_e2e:
-        xp, bp, kp = x_h.pin_memory(), b_h.pin_memory(), k_h.pin_memory()
-        yp = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-
-        def e2e_step():
-            x.copy_(xp, non_blocking=True)
-            b.copy_(bp, non_blocking=True)
-            keep.copy_(kp, non_blocking=True)
-            step()
-            yp.copy_(y, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize()
+        host_in = [x_h.pin_memory(), b_h.pin_memory(), k_h.pin_memory()]
         n_e2e = max(3, min(args.steps, 10))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ems = max_over_ranks(e0.elapsed_time(e1), dev) / n_e2e
+
+        def ew_step(ins, outs, s):
+            fa.bias_gelu_dropout(ins[0], ins[1], ins[2], w.p, out=outs[0], stream=s)
+
+        ems = max_over_ranks(pipelined_e2e(n_e2e, host_in, (y,), ew_step), dev)
         e2e = {"value": nbytes * world / (ems * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ems, "steps": n_e2e,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (x, b, keep)),
-               "d2h_bytes_per_step": y.numel() * y.element_size()}
+               "d2h_bytes_per_step": y.numel() * y.element_size(), "overlap": E2E_OVERLAP}
 
     peaks, peak_src = load_peaks()
     peak = float(peaks["hbm_gbs"])
@@ -836,38 +882,21 @@ def main(argv=None):
     # ---- end to end through the public call with host buffers
     e2e = None
     if not args.no_e2e:
-        qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
-        op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        host_in = [t.pin_memory() for t in (q_h, k_h, v_h)]
 
-        def e2e_step():
-            q.copy_(qp, non_blocking=True)
-            k.copy_(kp, non_blocking=True)
-            v.copy_(vp, non_blocking=True)
-            fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
-            op.copy_(o, non_blocking=True)
-            lp.copy_(lse, non_blocking=True)
+        def fwd_step(ins, outs, s):
+            fa.fwd_into(*ins, *outs, w.causal, w.scale, stream=s)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 20))
         barrier()
         torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
+        ems = max_over_ranks(pipelined_e2e(n_e2e, host_in, (o, lse), fwd_step), dev)
         barrier()
-        ems = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": job_tflops(flops, world, ems / n_e2e), "unit": "TFLOP/s",
-               "ms_per_step": ems / n_e2e, "steps": n_e2e, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+        e2e = {"value": job_tflops(flops, world, ems), "unit": "TFLOP/s",
+               "ms_per_step": ems, "steps": n_e2e, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "overlap": E2E_OVERLAP}
 
     peaks, peak_src = load_peaks()
     achieved = flops / (ms_per_step * 1e-3) / 1e12
