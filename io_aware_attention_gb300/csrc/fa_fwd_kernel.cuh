@@ -642,351 +642,156 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // contiguous): 64-column blocks BLK_BYTES apart (the ones block follows
         // the value blocks), 8-key groups 1024 bytes apart.
         if constexpr (L::SPLIT) {
-        // [O_h | l~_h] (+)= P_h [V_h | 1] for global tile g and each half h:
-        // A = P_h from TMEM (over the half's scores in S buffer g & 1; 2 bf16
-        // per column, 8 columns per 16 keys), B = value rows 64h .. 64h+63,
-        // MN-major (value columns contiguous): 64-column blocks BLK_BYTES
-        // apart (the ones block follows the value blocks), 8-key groups 1024
-        // bytes apart.  Each half's P is taken as soon as it is written.
-        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
-        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
-        int g = 0, k = 0;  // tiles and items done
-        bool ok = true;
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
-            const int n = item_of<CAUSAL>(i, p).n_kv;
-            // The first P.V of an item overwrites O: wait until the softmax
-            // warps have read out the previous item's O.
-            if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
-                                     0x200 + L::B_OFREE)))
-                break;
-            for (int j = 0; ok && j < n; ++j, ++g) {
-                const int s = g % L::VSTAGES;
-                const int b = g & 1;
-                // V of tile g, loaded long before, is checked first: an mbarrier
-                // check is slow while the score MMAs stream their operands, and
-                // it then overlaps the softmax warps' work on P.
-                if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
-                                         abort_flag, 0x200 + L::B_VFULL + s)))
+            // [O_h | l~_h] (+)= P_h [V_h | 1] for global tile g and each half h:
+            // A = P_h from TMEM (over the half's scores in S buffer g & 1; 2 bf16
+            // per column, 8 columns per 16 keys), B = value rows 64h .. 64h+63,
+            // MN-major (value columns contiguous): 64-column blocks BLK_BYTES
+            // apart (the ones block follows the value blocks), 8-key groups 1024
+            // bytes apart.  Each half's P is taken as soon as it is written.
+            constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
+            const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
+            int g = 0, k = 0;  // tiles and items done
+            bool ok = true;
+            for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+                const int n = item_of<CAUSAL>(i, p).n_kv;
+                // The first P.V of an item overwrites O: wait until the softmax
+                // warps have read out the previous item's O.
+                if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                         0x200 + L::B_OFREE)))
                     break;
-                if (lane == 0) FA_TRACE_EV(10, g, 3);
-                const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
-                const uint32_t s_tm = tmem + (b ? TM_S1 : TM_S0);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // P_h of tile g (per S buffer: the phase before, tile g - 2,
-                    // was consumed by this warp, so parity cannot alias).
-                    if (!(ok = warp_wait_bar(bar(L::B_PFULL + 2 * h + b), (uint32_t)(g >> 1) & 1u, limit,
-                                             abort_flag, 0x200 + L::B_PFULL + 2 * h + b)))
+                for (int j = 0; ok && j < n; ++j, ++g) {
+                    const int s = g % L::VSTAGES;
+                    const int b = g & 1;
+                    // V of tile g, loaded long before, is checked first: an mbarrier
+                    // check is slow while the score MMAs stream their operands, and
+                    // it then overlaps the softmax warps' work on P.
+                    if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
+                                             abort_flag, 0x200 + L::B_VFULL + s)))
                         break;
-                    ptx::tc_fence_after_sync();
+                    if (lane == 0) FA_TRACE_EV(10, g, 3);
+                    const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
+                    const uint32_t s_tm = tmem + (b ? TM_S1 : TM_S0);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (ptx::elect_one())
-                            ptx::mma_ts(tmem + TM_O + (uint32_t)h * L::O_STRIDE, s_tm + (uint32_t)(h * 64 + kk * 8),
-                                        v_desc + (uint64_t)(((h * 64 + kk * 16) * 128) >> 4), IDESC_O,
-                                        (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        // P_h of tile g (per S buffer: the phase before, tile g - 2,
+                        // was consumed by this warp, so parity cannot alias).
+                        if (!(ok = warp_wait_bar(bar(L::B_PFULL + 2 * h + b), (uint32_t)(g >> 1) & 1u, limit,
+                                                 abort_flag, 0x200 + L::B_PFULL + 2 * h + b)))
+                            break;
+                        ptx::tc_fence_after_sync();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (ptx::elect_one())
+                                ptx::mma_ts(tmem + TM_O + (uint32_t)h * L::O_STRIDE, s_tm + (uint32_t)(h * 64 + kk * 8),
+                                            v_desc + (uint64_t)(((h * 64 + kk * 16) * 128) >> 4), IDESC_O,
+                                            (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    if (!ok) break;
+                    if (ptx::elect_one()) {
+                        // The commits cover every MMA this warp issued so far.
+                        ptx::tc_commit(bar(L::B_VEMPTY + s));
+                        ptx::tc_commit(bar(L::B_ODONE + b));
+                        if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
+                        FA_TRACE_EV(10, g, 4);
                     }
                 }
-                if (!ok) break;
-                if (ptx::elect_one()) {
-                    // The commits cover every MMA this warp issued so far.
-                    ptx::tc_commit(bar(L::B_VEMPTY + s));
-                    ptx::tc_commit(bar(L::B_ODONE + b));
-                    if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
-                    FA_TRACE_EV(10, g, 4);
-                }
             }
-        }
         } else {
-        constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
-        const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
-        const uint32_t p_tmem = tmem + TM_P;
-        int g = 0, k = 0;  // tiles and items done
-        bool ok = true;
-        for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
-            const int n = item_of<CAUSAL>(i, p).n_kv;
-            // The first P.V of an item overwrites O: wait until the softmax
-            // warps have read out the previous item's O.
-            if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
-                                     0x200 + L::B_OFREE)))
-                break;
-            for (int j = 0; j < n; ++j, ++g) {
-                const int s = g % L::VSTAGES;
-                // V of tile g, loaded long before, is checked first: an mbarrier
-                // check is slow while the score MMAs stream their operands, and
-                // it then overlaps the softmax warps' work on P.  Then P of tile
-                // g (the phase before is P of g - 1, which this warp has
-                // consumed, so parity cannot alias).
-                if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
-                                         abort_flag, 0x200 + L::B_VFULL + s)))
+            constexpr uint32_t IDESC_O = ptx::idesc_bf16_f32(BM, D + 16, true);
+            const uint64_t v_desc0 = ptx::sdesc_sw128(sbase + L::OFF_V, BLK_BYTES, 1024);
+            const uint32_t p_tmem = tmem + TM_P;
+            int g = 0, k = 0;  // tiles and items done
+            bool ok = true;
+            for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step), ++k) {
+                const int n = item_of<CAUSAL>(i, p).n_kv;
+                // The first P.V of an item overwrites O: wait until the softmax
+                // warps have read out the previous item's O.
+                if (!(ok = warp_wait_bar(bar(L::B_OFREE), (uint32_t)(k & 1) ^ 1u, limit, abort_flag,
+                                         0x200 + L::B_OFREE)))
                     break;
-                if (lane == 0) FA_TRACE_EV(10, g, 3);
-                if (!(ok = warp_wait_bar(bar(L::B_PFULL), (uint32_t)(g & 1), limit, abort_flag,
-                                         0x200 + L::B_PFULL)))
-                    break;
-                if (lane == 0) FA_TRACE_EV(10, g, 2);
-                ptx::tc_fence_after_sync();
-                const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
+                for (int j = 0; j < n; ++j, ++g) {
+                    const int s = g % L::VSTAGES;
+                    // V of tile g, loaded long before, is checked first: an mbarrier
+                    // check is slow while the score MMAs stream their operands, and
+                    // it then overlaps the softmax warps' work on P.  Then P of tile
+                    // g (the phase before is P of g - 1, which this warp has
+                    // consumed, so parity cannot alias).
+                    if (!(ok = warp_wait_bar(bar(L::B_VFULL + s), (uint32_t)(g / L::VSTAGES) & 1u, limit,
+                                             abort_flag, 0x200 + L::B_VFULL + s)))
+                        break;
+                    if (lane == 0) FA_TRACE_EV(10, g, 3);
+                    if (!(ok = warp_wait_bar(bar(L::B_PFULL), (uint32_t)(g & 1), limit, abort_flag,
+                                             0x200 + L::B_PFULL)))
+                        break;
+                    if (lane == 0) FA_TRACE_EV(10, g, 2);
+                    ptx::tc_fence_after_sync();
+                    const uint64_t v_desc = v_desc0 + (uint64_t)((s * L::VSTAGE) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    if (ptx::elect_one())
-                        ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
-                                    v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    if (kk == 0 && lane == 0) FA_TRACE_EV(10, g, 5);
-                    if (kk == 7 && lane == 0) FA_TRACE_EV(10, g, 7);
-                }
-                if (ptx::elect_one()) {
-                    ptx::tc_commit(bar(L::B_VEMPTY + s));
-                    ptx::tc_commit(bar(L::B_ODONE));
-                    if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
-                    FA_TRACE_EV(10, g, 4);
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        if (ptx::elect_one())
+                            ptx::mma_ts(tmem + TM_O, p_tmem + (uint32_t)kk * 8,
+                                        v_desc + (uint64_t)(kk * ((16 * 128) >> 4)), IDESC_O,
+                                        (j > 0 || kk > 0) ? 1u : 0u);
+                        if (kk == 0 && lane == 0) FA_TRACE_EV(10, g, 5);
+                        if (kk == 7 && lane == 0) FA_TRACE_EV(10, g, 7);
+                    }
+                    if (ptx::elect_one()) {
+                        ptx::tc_commit(bar(L::B_VEMPTY + s));
+                        ptx::tc_commit(bar(L::B_ODONE));
+                        if (j == n - 1) ptx::tc_commit(bar(L::B_OFINAL));
+                        FA_TRACE_EV(10, g, 4);
+                    }
                 }
             }
-        }
         }
         if (ptx::elect_one()) ptx::tc_commit(bar(L::B_DRAIN + 1));
         drain_bar(bar(L::B_DRAIN + 1), 0, limit, abort_flag, 0x281);
     } else {
-      if constexpr (L::SPLIT) {
-        // ------------------------------------- softmax warps, split design
-        // Warp w serves query rows 32*(w%4) .. +31 (its TMEM lane quarter) and
-        // score columns 64*h .. +63, h = w/4, with a state of its own: its
-        // reference max, its row sum, its P (written over its half of the S
-        // buffer) and its accumulator [O_h | l~_h] = sum over tiles of
-        // P_h [V_h | 1].  The two halves of a row meet once per item, in the
-        // epilogue.
-        const int quarter = warp & 3;
-        const int half = warp >> 2;
-        const int row = quarter * 32 + lane;      // query row in the item == TMEM lane
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t o_mine = tmem + lane_off + TM_O + (uint32_t)half * L::O_STRIDE;
-        const float sl2 = p.scale_log2;
-        const uint32_t nb_sready = NB_SREADY_SPLIT0 + 3u * (uint32_t)half;
-        float* const xch = reinterpret_cast<float*>(sgen + L::OFF_XCH);
-        bool ok = true;
-        int g = 0;      // tiles done
-        int kitem = 0;  // items done
+        if constexpr (L::SPLIT) {
+            // ------------------------------------- softmax warps, split design
+            // Warp w serves query rows 32*(w%4) .. +31 (its TMEM lane quarter) and
+            // score columns 64*h .. +63, h = w/4, with a state of its own: its
+            // reference max, its row sum, its P (written over its half of the S
+            // buffer) and its accumulator [O_h | l~_h] = sum over tiles of
+            // P_h [V_h | 1].  The two halves of a row meet once per item, in the
+            // epilogue.
+            const int quarter = warp & 3;
+            const int half = warp >> 2;
+            const int row = quarter * 32 + lane;      // query row in the item == TMEM lane
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const uint32_t o_mine = tmem + lane_off + TM_O + (uint32_t)half * L::O_STRIDE;
+            const float sl2 = p.scale_log2;
+            const uint32_t nb_sready = NB_SREADY_SPLIT0 + 3u * (uint32_t)half;
+            float* const xch = reinterpret_cast<float*>(sgen + L::OFF_XCH);
+            bool ok = true;
+            int g = 0;      // tiles done
+            int kitem = 0;  // items done
 
-        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
-            const Item it = item_of<CAUSAL>(i, p);
-            const int q_idx = it.q0 + row;
-            const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
-            const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
-            float m_ref = -INFINITY;
-            // This half-row's sum of probabilities, as four packed fp32 pairs.
-            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
-            {
-            // This half-row's scores (fp32 bit patterns), used in place: the
-            // packed fp32x2 arithmetic takes neighbouring load registers as
-            // its operand pairs.
-            uint32_t sr[64];
+            for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
+                const Item it = item_of<CAUSAL>(i, p);
+                const int q_idx = it.q0 + row;
+                const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
+                const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
+                float m_ref = -INFINITY;
+                // This half-row's sum of probabilities, as four packed fp32 pairs.
+                uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+                {
+                // This half-row's scores (fp32 bit patterns), used in place: the
+                // packed fp32x2 arithmetic takes neighbouring load registers as
+                // its operand pairs.
+                uint32_t sr[64];
 
-            for (int j = 0; j < it.n_kv; ++j, ++g) {
-                const int b = g & 1;
-                const uint32_t s_half = tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64;
-                // S of tile g is in TMEM (met on every tile, also after an abort).
-                ptx::named_barrier_sync(nb_sready + (uint32_t)(g % 3), NB_SREADY_SPLIT_COUNT);
-                if (!ok) continue;
-                ptx::tc_fence_after_sync();
-                ptx::tmem_ld64(s_half, sr);
-                if (lane == 0) FA_TRACE_EV(warp, g, 0);
-                ptx::tmem_wait_ld64(sr);
-                if (lane == 0) FA_TRACE_EV(warp, g, 1);
-                // Causal diagonal tile / keys past N: -inf before the max.
-                const int k0 = j * BN + half * 64;
-                if (j * BN + BN - 1 > cta_key_max) {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
-                }
-                const float m_tile = max64(sr) * sl2;  // scale > 0, so max commutes with it
-                if (lane == 0) FA_TRACE_EV(warp, g, 2);
-
-                // A half-row may have no visible key yet (its reference then
-                // stays -inf and its P, O_h and l are 0).
-                if (j == 0) {
-                    m_ref = m_tile;
-                } else {
-                    const float m_new = fmaxf(m_ref, m_tile);
-                    const bool need = m_new > m_ref + RESCALE_LOG2;
-                    if (__any_sync(0xffffffffu, need)) {
-                        // O_h holds everything up to the previous tile once
-                        // both halves' P.V of it are done (the phase before,
-                        // tile g - 3, cannot alias: tile g - 1 was issued only
-                        // after it).
-                        if (!(ok = warp_wait_bar(bar(L::B_ODONE + ((g - 1) & 1)), (uint32_t)((g - 1) >> 1) & 1u,
-                                                 limit, abort_flag, 0x300 + L::B_ODONE + ((g - 1) & 1))))
-                            continue;
-                        ptx::tc_fence_after_sync();
-                        const float corr = ptx::ex2(m_ref - m_new);
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
-
-                        m_ref = m_new;
-                        scale_row<D>(o_mine, corr);
-                        uint32_t lt[8];
-                        ptx::tmem_ld8(o_mine + D, lt);
-                        ptx::tmem_wait_ld_only();
-                        ptx::reg_fence8(lt);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) lt[c] = __float_as_uint(__uint_as_float(lt[c]) * corr);
-                        ptx::tmem_st8(o_mine + D, lt);
-                        ptx::tmem_wait_st();
-                    }
-                }
-
-                // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
-                // scaling and the sums use packed fp32x2 instructions: fewer
-                // issue slots, which the MMA issuers on the same sub-partitions
-                // need.
-                const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
-                const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-                const uint64_t neg_m2 = ptx::f2_pack(-m_use, -m_use);
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float x0, x1;
-                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
-                                               sl2x2, neg_m2),
-                                   x0, x1);
-                    const float a0 = ptx::ex2(x0);
-                    const float a1 = ptx::ex2(x1);
-                    lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
-                    pk[c] = ptx::pack_bf16x2(a0, a1);
-                }
-                if (lane == 0) FA_TRACE_EV(warp, g, 3);
-
-                // P over this half's scores (read into registers above).
-                ptx::tmem_st32(s_half, pk);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + 2 * half + b));
-                if (lane == 0) FA_TRACE_EV(warp, g, 5);
-            }
-            }
-
-            // --------------------------------------------------- epilogue
-            // With w_h = 2^(m_h - M), M = max(m_0, m_1):
-            //   O   = (w_0 O_0 + w_1 O_1) / (w_0 l~_0 + w_1 l~_1)   (l~: sums of the rounded P)
-            //   lse = (M + log2(w_0 l_0 + w_1 l_1)) ln 2            (l: sums of the fp32 P)
-            // The two halves' (m, l, l~) meet through shared memory (one
-            // slot per item parity, so the next item's write never meets this
-            // item's read).
-            if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
-                                       0x380 + L::B_OFINAL);
-            float l_lo, l_hi;
-            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
-            const float l_mine = l_lo + l_hi;
-            float lr_mine = 0.f;
-            if (ok) {
-                ptx::tc_fence_after_sync();
-                uint32_t lt[8];
-                ptx::tmem_ld8(o_mine + D, lt);
-                ptx::tmem_wait_ld_only();
-                ptx::reg_fence8(lt);
-                lr_mine = __uint_as_float(lt[0]);
-            }
-            float* const slot = xch + (kitem & 1) * (6 * BM);
-            slot[(3 * half) * BM + row] = m_ref;
-            slot[(3 * half + 1) * BM + row] = l_mine;
-            slot[(3 * half + 2) * BM + row] = lr_mine;
-            ++kitem;
-            ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
-            if (ok) {
-                const float m_other = slot[(3 * (half ^ 1)) * BM + row];
-                const float l_other = slot[(3 * (half ^ 1) + 1) * BM + row];
-                const float lr_other = slot[(3 * (half ^ 1) + 2) * BM + row];
-                const float m_max = fmaxf(m_ref, m_other);
-                const float s_mine = ptx::ex2(m_ref - m_max);
-                const float s_other = ptx::ex2(m_other - m_max);
-                const float l = l_mine * s_mine + l_other * s_other;
-                const float inv_l = 1.0f / (lr_mine * s_mine + lr_other * s_other);
-                const float s0 = (half == 0 ? s_mine : s_other) * inv_l;
-                const float s1 = (half == 0 ? s_other : s_mine) * inv_l;
-                const bool row_ok = q_idx < N;
-                // A head size d below D was zero-padded by the TMA loads: the
-                // padded columns of O are zero and not stored.
-                __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
-                const uint32_t o0 = tmem + lane_off + TM_O + (uint32_t)half * (D / 2);
-#pragma unroll
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    uint32_t oa[32], ob[32];
-                    ptx::tmem_ld32(o0 + ch * 32, oa);
-                    ptx::tmem_ld32(o0 + L::O_STRIDE + ch * 32, ob);
-                    ptx::tmem_wait_ld(oa);
-                    ptx::reg_fence(ob);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        w[c] = ptx::pack_bf16x2(
-                            fmaf(__uint_as_float(oa[2 * c]), s0, __uint_as_float(ob[2 * c]) * s1),
-                            fmaf(__uint_as_float(oa[2 * c + 1]), s0, __uint_as_float(ob[2 * c + 1]) * s1));
-                    if (row_ok) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
-                                ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                  w[4 * u + 3]);
-                    }
-                }
-                if (half == 0 && row_ok)
-                    p.lse[(int64_t)it.bh * N + q_idx] = (m_max + ptx::lg2(l)) * 0.69314718055994530942f;
-                // O has been read: the next item's first P.V may overwrite it.
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
-            }
-        }
-      } else {
-        // ---------------------------------------------------- softmax warps
-        const int quarter = warp & 3;
-        const int half = warp >> 2;               // score columns [64*half, 64*half+64)
-        const int row = quarter * 32 + lane;      // query row in the item == TMEM lane
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t o_cols = tmem + lane_off + TM_O + (uint32_t)half * (D / 2);
-        const uint32_t l_cols = tmem + lane_off + L::TM_L + (uint32_t)half * 8;
-        const float sl2 = p.scale_log2;
-        bool ok = true;
-        int g = 0;      // tiles done
-        int kitem = 0;  // items done
-
-        // Every softmax warp runs the same items and tiles and reaches each
-        // named barrier the same number of times, also after an abort
-        // (ok == false: the work is skipped, the barriers are not), so a named
-        // barrier never waits for a warp that has left the loop.
-        for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
-            const Item it = item_of<CAUSAL>(i, p);
-            const int q_idx = it.q0 + row;
-            const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
-            const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
-            float m_ref = -INFINITY;
-            // This half-row's sum of probabilities, as four packed fp32 pairs.
-            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
-            {
-            // This half-row's scores (fp32 bit patterns), used in place: the
-            // packed fp32x2 arithmetic takes neighbouring load registers as
-            // its operand pairs.
-            uint32_t sr[64];
-
-            for (int j = 0; j < it.n_kv; ++j, ++g) {
-                const int b = g & 1;
-                // S of tile g is in TMEM (met on every tile, also after an abort).
-                ptx::named_barrier_sync(NB_SREADY0 + (uint32_t)(g % 3), NB_SREADY_COUNT);
-                if (ok) {
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    const int b = g & 1;
+                    const uint32_t s_half = tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64;
+                    // S of tile g is in TMEM (met on every tile, also after an abort).
+                    ptx::named_barrier_sync(nb_sready + (uint32_t)(g % 3), NB_SREADY_SPLIT_COUNT);
+                    if (!ok) continue;
                     ptx::tc_fence_after_sync();
-                    ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
-                }
-                if (lane == 0) FA_TRACE_EV(warp, g, 0);
-                float mx = -INFINITY;
-                if (ok) {
+                    ptx::tmem_ld64(s_half, sr);
+                    if (lane == 0) FA_TRACE_EV(warp, g, 0);
                     ptx::tmem_wait_ld64(sr);
-                    // The scores are in registers: S of tile g + 2 may now be
-                    // written into this buffer.
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(L::B_SREAD + b));
                     if (lane == 0) FA_TRACE_EV(warp, g, 1);
                     // Causal diagonal tile / keys past N: -inf before the max.
                     const int k0 = j * BN + half * 64;
@@ -995,153 +800,349 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int c = 0; c < 64; ++c)
                             if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
                     }
-                    mx = max64(sr);
-                    ptx::tmem_st1(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + half), __float_as_uint(mx));
+                    const float m_tile = max64(sr) * sl2;  // scale > 0, so max commutes with it
+                    if (lane == 0) FA_TRACE_EV(warp, g, 2);
+
+                    // A half-row may have no visible key yet (its reference then
+                    // stays -inf and its P, O_h and l are 0).
+                    if (j == 0) {
+                        m_ref = m_tile;
+                    } else {
+                        const float m_new = fmaxf(m_ref, m_tile);
+                        const bool need = m_new > m_ref + RESCALE_LOG2;
+                        if (__any_sync(0xffffffffu, need)) {
+                            // O_h holds everything up to the previous tile once
+                            // both halves' P.V of it are done (the phase before,
+                            // tile g - 3, cannot alias: tile g - 1 was issued only
+                            // after it).
+                            if (!(ok = warp_wait_bar(bar(L::B_ODONE + ((g - 1) & 1)), (uint32_t)((g - 1) >> 1) & 1u,
+                                                     limit, abort_flag, 0x300 + L::B_ODONE + ((g - 1) & 1))))
+                                continue;
+                            ptx::tc_fence_after_sync();
+                            const float corr = ptx::ex2(m_ref - m_new);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
+
+                            m_ref = m_new;
+                            scale_row<D>(o_mine, corr);
+                            uint32_t lt[8];
+                            ptx::tmem_ld8(o_mine + D, lt);
+                            ptx::tmem_wait_ld_only();
+                            ptx::reg_fence8(lt);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) lt[c] = __float_as_uint(__uint_as_float(lt[c]) * corr);
+                            ptx::tmem_st8(o_mine + D, lt);
+                            ptx::tmem_wait_st();
+                        }
+                    }
+
+                    // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
+                    // scaling and the sums use packed fp32x2 instructions: fewer
+                    // issue slots, which the MMA issuers on the same sub-partitions
+                    // need.
+                    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+                    const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+                    const uint64_t neg_m2 = ptx::f2_pack(-m_use, -m_use);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float x0, x1;
+                        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                                   sl2x2, neg_m2),
+                                       x0, x1);
+                        const float a0 = ptx::ex2(x0);
+                        const float a1 = ptx::ex2(x1);
+                        lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
+                        pk[c] = ptx::pack_bf16x2(a0, a1);
+                    }
+                    if (lane == 0) FA_TRACE_EV(warp, g, 3);
+
+                    // P over this half's scores (read into registers above).
+                    ptx::tmem_st32(s_half, pk);
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL + 2 * half + b));
+                    if (lane == 0) FA_TRACE_EV(warp, g, 5);
+                }
+                }
+
+                // --------------------------------------------------- epilogue
+                // With w_h = 2^(m_h - M), M = max(m_0, m_1):
+                //   O   = (w_0 O_0 + w_1 O_1) / (w_0 l~_0 + w_1 l~_1)   (l~: sums of the rounded P)
+                //   lse = (M + log2(w_0 l_0 + w_1 l_1)) ln 2            (l: sums of the fp32 P)
+                // The two halves' (m, l, l~) meet through shared memory (one
+                // slot per item parity, so the next item's write never meets this
+                // item's read).
+                if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
+                                           0x380 + L::B_OFINAL);
+                float l_lo, l_hi;
+                ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
+                const float l_mine = l_lo + l_hi;
+                float lr_mine = 0.f;
+                if (ok) {
+                    ptx::tc_fence_after_sync();
+                    uint32_t lt[8];
+                    ptx::tmem_ld8(o_mine + D, lt);
+                    ptx::tmem_wait_ld_only();
+                    ptx::reg_fence8(lt);
+                    lr_mine = __uint_as_float(lt[0]);
+                }
+                float* const slot = xch + (kitem & 1) * (6 * BM);
+                slot[(3 * half) * BM + row] = m_ref;
+                slot[(3 * half + 1) * BM + row] = l_mine;
+                slot[(3 * half + 2) * BM + row] = lr_mine;
+                ++kitem;
+                ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
+                if (ok) {
+                    const float m_other = slot[(3 * (half ^ 1)) * BM + row];
+                    const float l_other = slot[(3 * (half ^ 1) + 1) * BM + row];
+                    const float lr_other = slot[(3 * (half ^ 1) + 2) * BM + row];
+                    const float m_max = fmaxf(m_ref, m_other);
+                    const float s_mine = ptx::ex2(m_ref - m_max);
+                    const float s_other = ptx::ex2(m_other - m_max);
+                    const float l = l_mine * s_mine + l_other * s_other;
+                    const float inv_l = 1.0f / (lr_mine * s_mine + lr_other * s_other);
+                    const float s0 = (half == 0 ? s_mine : s_other) * inv_l;
+                    const float s1 = (half == 0 ? s_other : s_mine) * inv_l;
+                    const bool row_ok = q_idx < N;
+                    // A head size d below D was zero-padded by the TMA loads: the
+                    // padded columns of O are zero and not stored.
+                    __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
+                    const uint32_t o0 = tmem + lane_off + TM_O + (uint32_t)half * (D / 2);
+#pragma unroll
+                    for (int ch = 0; ch < D / 64; ++ch) {
+                        uint32_t oa[32], ob[32];
+                        ptx::tmem_ld32(o0 + ch * 32, oa);
+                        ptx::tmem_ld32(o0 + L::O_STRIDE + ch * 32, ob);
+                        ptx::tmem_wait_ld(oa);
+                        ptx::reg_fence(ob);
+                        uint32_t w[16];
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            w[c] = ptx::pack_bf16x2(
+                                fmaf(__uint_as_float(oa[2 * c]), s0, __uint_as_float(ob[2 * c]) * s1),
+                                fmaf(__uint_as_float(oa[2 * c + 1]), s0, __uint_as_float(ob[2 * c + 1]) * s1));
+                        if (row_ok) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
+                                    ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                      w[4 * u + 3]);
+                        }
+                    }
+                    if (half == 0 && row_ok)
+                        p.lse[(int64_t)it.bh * N + q_idx] = (m_max + ptx::lg2(l)) * 0.69314718055994530942f;
+                    // O has been read: the next item's first P.V may overwrite it.
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
+                }
+            }
+        } else {
+            // ---------------------------------------------------- softmax warps
+            const int quarter = warp & 3;
+            const int half = warp >> 2;               // score columns [64*half, 64*half+64)
+            const int row = quarter * 32 + lane;      // query row in the item == TMEM lane
+            const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+            const uint32_t o_cols = tmem + lane_off + TM_O + (uint32_t)half * (D / 2);
+            const uint32_t l_cols = tmem + lane_off + L::TM_L + (uint32_t)half * 8;
+            const float sl2 = p.scale_log2;
+            bool ok = true;
+            int g = 0;      // tiles done
+            int kitem = 0;  // items done
+
+            // Every softmax warp runs the same items and tiles and reaches each
+            // named barrier the same number of times, also after an abort
+            // (ok == false: the work is skipped, the barriers are not), so a named
+            // barrier never waits for a warp that has left the loop.
+            for (int i = first_item(), step = 0; i < p.num_items; i = next_item(i, step)) {
+                const Item it = item_of<CAUSAL>(i, p);
+                const int q_idx = it.q0 + row;
+                const int key_max = CAUSAL ? min(q_idx, N - 1) : N - 1;
+                const int cta_key_max = CAUSAL ? min(it.q0, N - 1) : N - 1;  // smallest key_max of the item
+                float m_ref = -INFINITY;
+                // This half-row's sum of probabilities, as four packed fp32 pairs.
+                uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};
+                {
+                // This half-row's scores (fp32 bit patterns), used in place: the
+                // packed fp32x2 arithmetic takes neighbouring load registers as
+                // its operand pairs.
+                uint32_t sr[64];
+
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    const int b = g & 1;
+                    // S of tile g is in TMEM (met on every tile, also after an abort).
+                    ptx::named_barrier_sync(NB_SREADY0 + (uint32_t)(g % 3), NB_SREADY_COUNT);
+                    if (ok) {
+                        ptx::tc_fence_after_sync();
+                        ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
+                    }
+                    if (lane == 0) FA_TRACE_EV(warp, g, 0);
+                    float mx = -INFINITY;
+                    if (ok) {
+                        ptx::tmem_wait_ld64(sr);
+                        // The scores are in registers: S of tile g + 2 may now be
+                        // written into this buffer.
+                        ptx::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(L::B_SREAD + b));
+                        if (lane == 0) FA_TRACE_EV(warp, g, 1);
+                        // Causal diagonal tile / keys past N: -inf before the max.
+                        const int k0 = j * BN + half * 64;
+                        if (j * BN + BN - 1 > cta_key_max) {
+#pragma unroll
+                            for (int c = 0; c < 64; ++c)
+                                if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
+                        }
+                        mx = max64(sr);
+                        ptx::tmem_st1(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + half), __float_as_uint(mx));
+                        ptx::tmem_wait_st();
+                        ptx::tc_fence_before_sync();
+                    }
+                    // Row max: this half's, then the partner warp's through two TMEM
+                    // columns per S buffer (TMEM, unlike shared memory, does not
+                    // queue behind the score MMAs' operand reads).  The slot is
+                    // rewritten two tiles later, after the partner has passed the
+                    // next tile's barrier, so after it read this value.
+                    ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
+                    if (lane == 0) FA_TRACE_EV(warp, g, 2);
+                    if (!ok) continue;
+                    ptx::tc_fence_after_sync();
+                    const uint32_t mx_other = tmem + lane_off + TM_MX + (uint32_t)(b * 2 + (half ^ 1));
+                    mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1_wait(mx_other)));
+                    const float m_tile = mx * sl2;  // scale > 0, so max commutes with it
+
+                    // [O | l~] and the P buffer are free of tile g - 1 once its P.V
+                    // is done (O_DONE; the phase before, P.V of g - 2, was waited
+                    // for before P of g - 1 was written, so parity cannot alias).
+                    bool o_done = g == 0;
+                    auto wait_o_done = [&]() -> bool {
+                        if (o_done) return true;
+                        if (!warp_wait_bar(bar(L::B_ODONE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
+                                           0x300 + L::B_ODONE))
+                            return false;
+                        ptx::tc_fence_after_sync();
+                        o_done = true;
+                        return true;
+                    };
+                    if (j == 0) {
+                        m_ref = (m_tile == -INFINITY) ? 0.f : m_tile;
+                    } else {
+                        const float m_new = fmaxf(m_ref, m_tile);
+                        const bool need = m_new > m_ref + RESCALE_LOG2;
+                        // Both halves of a row see the same values, so they decide alike.
+                        if (__any_sync(0xffffffffu, need)) {
+                            // [O | l~] hold everything up to the previous tile once
+                            // its P.V is done.
+                            if (!(ok = wait_o_done())) continue;
+                            const float corr = ptx::ex2(m_ref - m_new);
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
+                            m_ref = m_new;
+                            scale_cols<D>(o_cols, corr);
+                            uint32_t lt[8];
+                            ptx::tmem_ld8(l_cols, lt);
+                            ptx::tmem_wait_ld_only();
+                            ptx::reg_fence8(lt);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) lt[c] = __float_as_uint(__uint_as_float(lt[c]) * corr);
+                            ptx::tmem_st8(l_cols, lt);
+                            ptx::tmem_wait_st();
+                        }
+                    }
+
+                    // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
+                    // scaling and the sums use packed fp32x2 instructions: fewer
+                    // issue slots, which the MMA issuer on the same sub-partition
+                    // needs.
+                    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+                    const uint64_t neg_m2 = ptx::f2_pack(-m_ref, -m_ref);
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float x0, x1;
+                        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                                   sl2x2, neg_m2),
+                                       x0, x1);
+                        const float a0 = ptx::ex2(x0);
+                        const float a1 = ptx::ex2(x1);
+                        lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
+                        pk[c] = ptx::pack_bf16x2(a0, a1);
+                    }
+                    if (lane == 0) FA_TRACE_EV(warp, g, 3);
+
+                    // P into the P buffer once the previous tile's P.V has read it.
+                    if (!(ok = wait_o_done())) continue;
+                    ptx::tmem_st32(tmem + lane_off + TM_P + (uint32_t)half * 32, pk);
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL));
+                    if (lane == 0) FA_TRACE_EV(warp, g, 5);
+                }
+                }
+
+                // --------------------------------------------------- epilogue
+                // A wait on the per-tile barrier could be fooled by parity while an
+                // earlier P.V is still running; the per-item barrier cannot.
+                if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
+                                           0x380 + L::B_OFINAL);
+                ++kitem;
+                float l_lo, l_hi;
+                ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
+                const float l_half = l_lo + l_hi;
+                // The two halves' fp32 sums meet in two spare TMEM columns (all of
+                // this item's MMAs are complete).
+                if (ok) {
+                    ptx::tc_fence_after_sync();
+                    ptx::tmem_st1(tmem + lane_off + TM_LX + (uint32_t)half, __float_as_uint(l_half));
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before_sync();
                 }
-                // Row max: this half's, then the partner warp's through two TMEM
-                // columns per S buffer (TMEM, unlike shared memory, does not
-                // queue behind the score MMAs' operand reads).  The slot is
-                // rewritten two tiles later, after the partner has passed the
-                // next tile's barrier, so after it read this value.
                 ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
-                if (lane == 0) FA_TRACE_EV(warp, g, 2);
-                if (!ok) continue;
-                ptx::tc_fence_after_sync();
-                mx = fmaxf(mx, __uint_as_float(ptx::tmem_ld1_wait(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + (half ^ 1)))));
-                const float m_tile = mx * sl2;  // scale > 0, so max commutes with it
-
-                // [O | l~] and the P buffer are free of tile g - 1 once its P.V
-                // is done (O_DONE; the phase before, P.V of g - 2, was waited
-                // for before P of g - 1 was written, so parity cannot alias).
-                bool o_done = g == 0;
-                auto wait_o_done = [&]() -> bool {
-                    if (o_done) return true;
-                    if (!warp_wait_bar(bar(L::B_ODONE), (uint32_t)(g - 1) & 1u, limit, abort_flag,
-                                       0x300 + L::B_ODONE))
-                        return false;
+                if (ok) {
                     ptx::tc_fence_after_sync();
-                    o_done = true;
-                    return true;
-                };
-                if (j == 0) {
-                    m_ref = (m_tile == -INFINITY) ? 0.f : m_tile;
-                } else {
-                    const float m_new = fmaxf(m_ref, m_tile);
-                    const bool need = m_new > m_ref + RESCALE_LOG2;
-                    // Both halves of a row see the same values, so they decide alike.
-                    if (__any_sync(0xffffffffu, need)) {
-                        // [O | l~] hold everything up to the previous tile once
-                        // its P.V is done.
-                        if (!(ok = wait_o_done())) continue;
-                        const float corr = ptx::ex2(m_ref - m_new);
+                    uint32_t la, lb;
+                    ptx::tmem_ld2(tmem + lane_off + TM_LX, la, lb);
+                    uint32_t lt[8];
+                    ptx::tmem_ld8(l_cols, lt);
+                    ptx::tmem_wait_ld_only();
+                    ptx::reg_fence8(lt);
+                    asm volatile("" : "+r"(la), "+r"(lb));
+                    const float l = __uint_as_float(la) + __uint_as_float(lb);
+                    const float inv_l = 1.0f / __uint_as_float(lt[0]);
+                    const bool row_ok = q_idx < N;
+                    // A head size d below D was zero-padded by the TMA loads: the
+                    // padded columns of O are zero and not stored.
+                    __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) lsum[c] = ptx::f2_mul(lsum[c], ptx::f2_pack(corr, corr));
-                        m_ref = m_new;
-                        scale_cols<D>(o_cols, corr);
-                        uint32_t lt[8];
-                        ptx::tmem_ld8(l_cols, lt);
-                        ptx::tmem_wait_ld_only();
-                        ptx::reg_fence8(lt);
+                    for (int ch = 0; ch < D / 64; ++ch) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(o_cols + ch * 32, o);
+                        ptx::tmem_wait_ld(o);
+                        uint32_t w[16];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) lt[c] = __float_as_uint(__uint_as_float(lt[c]) * corr);
-                        ptx::tmem_st8(l_cols, lt);
-                        ptx::tmem_wait_st();
+                        for (int c = 0; c < 16; ++c)
+                            w[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                                    __uint_as_float(o[2 * c + 1]) * inv_l);
+                        if (row_ok) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
+                                    ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                      w[4 * u + 3]);
+                        }
                     }
+                    if (half == 0 && row_ok)
+                        p.lse[(int64_t)it.bh * N + q_idx] = (m_ref + ptx::lg2(l)) * 0.69314718055994530942f;
+                    // O has been read: the next item's first P.V may overwrite it.
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
                 }
-
-                // P = 2^(s*c - m_ref), rounded to bf16 for the P.V MMA.  The
-                // scaling and the sums use packed fp32x2 instructions: fewer
-                // issue slots, which the MMA issuer on the same sub-partition
-                // needs.
-                const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
-                const uint64_t neg_m2 = ptx::f2_pack(-m_ref, -m_ref);
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float x0, x1;
-                    ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
-                                               sl2x2, neg_m2),
-                                   x0, x1);
-                    const float a0 = ptx::ex2(x0);
-                    const float a1 = ptx::ex2(x1);
-                    lsum[c & 3] = ptx::f2_add(lsum[c & 3], ptx::f2_pack(a0, a1));
-                    pk[c] = ptx::pack_bf16x2(a0, a1);
-                }
-                if (lane == 0) FA_TRACE_EV(warp, g, 3);
-
-                // P into the P buffer once the previous tile's P.V has read it.
-                if (!(ok = wait_o_done())) continue;
-                ptx::tmem_st32(tmem + lane_off + TM_P + (uint32_t)half * 32, pk);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_PFULL));
-                if (lane == 0) FA_TRACE_EV(warp, g, 5);
-            }
-            }
-
-            // --------------------------------------------------- epilogue
-            // A wait on the per-tile barrier could be fooled by parity while an
-            // earlier P.V is still running; the per-item barrier cannot.
-            if (ok) ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
-                                       0x380 + L::B_OFINAL);
-            ++kitem;
-            float l_lo, l_hi;
-            ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo, l_hi);
-            const float l_half = l_lo + l_hi;
-            // The two halves' fp32 sums meet in two spare TMEM columns (all of
-            // this item's MMAs are complete).
-            if (ok) {
-                ptx::tc_fence_after_sync();
-                ptx::tmem_st1(tmem + lane_off + TM_LX + (uint32_t)half, __float_as_uint(l_half));
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before_sync();
-            }
-            ptx::named_barrier_sync(NB_PAIR0 + quarter, 64);
-            if (ok) {
-                ptx::tc_fence_after_sync();
-                uint32_t la, lb;
-                ptx::tmem_ld2(tmem + lane_off + TM_LX, la, lb);
-                uint32_t lt[8];
-                ptx::tmem_ld8(l_cols, lt);
-                ptx::tmem_wait_ld_only();
-                ptx::reg_fence8(lt);
-                asm volatile("" : "+r"(la), "+r"(lb));
-                const float l = __uint_as_float(la) + __uint_as_float(lb);
-                const float inv_l = 1.0f / __uint_as_float(lt[0]);
-                const bool row_ok = q_idx < N;
-                // A head size d below D was zero-padded by the TMA loads: the
-                // padded columns of O are zero and not stored.
-                __nv_bfloat16* const orow = p.o + ((int64_t)it.bh * N + q_idx) * (PAD ? p.d : D) + half * (D / 2);
-#pragma unroll
-                for (int ch = 0; ch < D / 64; ++ch) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(o_cols + ch * 32, o);
-                    ptx::tmem_wait_ld(o);
-                    uint32_t w[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        w[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                                __uint_as_float(o[2 * c + 1]) * inv_l);
-                    if (row_ok) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (!PAD || half * (D / 2) + ch * 32 + u * 8 < p.d)
-                                ptx::st_global_v4(orow + ch * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                                                  w[4 * u + 3]);
-                    }
-                }
-                if (half == 0 && row_ok)
-                    p.lse[(int64_t)it.bh * N + q_idx] = (m_ref + ptx::lg2(l)) * 0.69314718055994530942f;
-                // O has been read: the next item's first P.V may overwrite it.
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_OFREE));
             }
         }
-      }
     }
 
     ptx::tc_fence_before_sync();
