@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) attention forward: Python binding of the C ABI in include/fa.h.
+"""GB300 (sm_103a) IO-aware attention: Python binding of the C ABI in include/fa.h.
 
 Only argument marshalling happens here; every step of the computation runs in
 the CUDA kernels of ``libfa_gb300.so``.  There is no fallback: if the library
@@ -6,19 +6,27 @@ is missing or the device is not sm_103, calls raise.
 
     o, lse = io_aware_attention_gb300.fwd(q, k, v, causal=True)
 
-q, k, v: CUDA bf16 tensors of shape (B, H, N, d), contiguous, d in {64, 128}.
+q, k, v: CUDA bf16 tensors of shape (B, H, N, d), contiguous, d a multiple of
+8 from 8 to 128.
 Returns o (bf16, same shape) and lse (fp32, (B, H, N)), the natural-log
 logsumexp of each row's scaled, masked scores.
 
     dq, dk, dv = io_aware_attention_gb300.bwd(q, k, v, o, lse, do, causal=True)
 
-gives the gradients for the output gradient ``do`` (d in {64, 128}), recomputing the
-probabilities from ``lse``.
+gives the gradients for the output gradient ``do`` (the same head sizes),
+recomputing the probabilities from ``lse``.
+
+    o, lse = io_aware_attention_gb300.decode(q, k_cache, v_cache, causal=True)
+
+is split-KV decode of up to 8 query rows against a long cache (d 64 or 128).
 
     y = io_aware_attention_gb300.bias_gelu_dropout(x, bias, keep, p)
 
 is the fused elementwise chain (bias add, tanh GELU, dropout with a packed
 keep mask drawn by the caller) in one HBM read and one write.
+
+The ``*_into`` forms write into caller-provided tensors; their shapes, dtypes
+and devices are checked here, because the C ABI sees only pointers and sizes.
 """
 from __future__ import annotations
 
@@ -124,10 +132,28 @@ def _check(q, k, v):
         raise ValueError("q, k, v must be on one device")
 
 
+def _check_out(name, t, shape, dtype, device):
+    """An output tensor the kernels write: CUDA, contiguous, of exactly this
+    shape and dtype, on the inputs' device."""
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def fwd_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None):
-    """Runs the kernel into caller-provided ``o`` (bf16) and ``lse`` (fp32)."""
+    """Runs the kernel into caller-provided ``o`` (bf16, the shape of q) and
+    ``lse`` (fp32, (B, H, N))."""
+    import torch
+
     _check(q, k, v)
     B, H, N, d = (int(s) for s in q.shape)
+    _check_out("o", o, q.shape, torch.bfloat16, q.device)
+    _check_out("lse", lse, (B, H, N), torch.float32, q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     rc = library().fa_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
@@ -172,8 +198,11 @@ def bwd_into(q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False, s
     if not (q.shape == o.shape == do.shape == dq.shape):
         raise ValueError("o, do, dq, dk, dv must have the shape of q")
     B, H, N, d = (int(s) for s in q.shape)
-    if lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous() or tuple(lse.shape) != (B, H, N):
-        raise ValueError("lse must be a contiguous CUDA fp32 (B, H, N) tensor")
+    if not (q.device == o.device == do.device == dq.device == dk.device == dv.device):
+        raise ValueError("q, k, v, o, do, dq, dk, dv must be on one device")
+    _check_out("lse", lse, (B, H, N), torch.float32, q.device)
+    if not workspace.is_cuda or workspace.device != q.device or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     ws_bytes = workspace.numel() * workspace.element_size()
@@ -218,6 +247,10 @@ def bias_gelu_dropout(x, bias, keep=None, p: float = 0.0, out=None, stream=None)
             raise ValueError("keep must be a contiguous CUDA int32/uint32 tensor of mask words")
         if keep.numel() * 32 < rows * cols:
             raise ValueError("keep holds fewer bits than x has elements")
+    if (keep is not None and keep.device != x.device) or bias.device != x.device:
+        raise ValueError("x, bias and keep must be on one device")
+    if out is not None:
+        _check_out("out", out, x.shape, torch.bfloat16, x.device)
     y = torch.empty_like(x) if out is None else out
     vp = ctypes.c_void_p
     rc = library().fa_bias_gelu_dropout(vp(x.data_ptr()), vp(bias.data_ptr()),
@@ -251,11 +284,19 @@ def decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int, causal: boo
 
 
 def decode_into(q, k, v, o, lse, workspace, causal: bool = False, scale: float | None = None, stream=None):
-    """Decode attention into caller-provided o, lse and workspace (a CUDA
-    tensor of at least decode_workspace_bytes bytes, or None when that is 0)."""
+    """Decode attention into caller-provided o (bf16, the shape of q), lse
+    (fp32, (B, H, Nq)) and workspace (a CUDA tensor of at least
+    decode_workspace_bytes bytes, or None when that is 0)."""
+    import torch
+
     _check_decode(q, k, v)
     B, H, Nq, d = (int(s) for s in q.shape)
     Nk = int(k.shape[2])
+    _check_out("o", o, q.shape, torch.bfloat16, q.device)
+    _check_out("lse", lse, (B, H, Nq), torch.float32, q.device)
+    if workspace is not None and (not workspace.is_cuda or workspace.device != q.device
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
