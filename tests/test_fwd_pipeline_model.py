@@ -1,0 +1,496 @@
+"""Happens-before model of the attention-forward kernel's pipeline (CPU only).
+
+fa_fwd_kernel.cuh coordinates a TMA producer warp, a score-MMA issuer, a
+P.V-MMA issuer and eight softmax warps through mbarriers (waited on by
+parity), hardware named barriers and the asynchronous completion of TMA
+copies and tcgen05 MMAs.  This test replays every role's sequence of barrier
+operations and buffer accesses in the order the kernel executes them, under
+random interleavings and random completion times of the copies and MMAs, and
+checks:
+
+* no data race: every two conflicting accesses to a buffer (the Q, K and V
+  stages in shared memory; the S, P and O regions of TMEM per lane quarter
+  and half row; the row-max, row-sum and epilogue exchange slots) are ordered
+  by happens-before.  Vector clocks travel through mbarrier phases, named
+  barrier generations, MMA commits and TMA completions; MMAs issued by one
+  thread execute in order;
+* parity safety: a wait for phase n of an mbarrier (parity n mod 2) starts
+  with at least n phases complete and returns before phase n + 1 completes,
+  so the parity cannot alias;
+* every arrival lands in the phase it is meant for, on mbarriers and named
+  barriers (no overrun), and no named-barrier generation is left incomplete;
+* no deadlock.
+
+Both designs are modelled: d = 128 (one softmax state per row split over two
+warps, a P buffer, S released once read) and the d = 64 split design (two
+independent half-row states, P over S, S released once P.V is done).  Planted
+protocol mistakes -- each a single wait or barrier left out -- are caught,
+which shows that the check can fail.  Only the healthy path is modelled; the
+abort path of the named barriers is checked in test_barrier_protocol.py.
+"""
+import random
+
+import pytest
+
+KSTAGES = {128: 3, 64: 4}
+VSTAGES = {128: 2, 64: 4}
+WARPS = 8  # softmax warps: warp w serves lane quarter w % 4, half row w // 4
+
+
+class Violation(Exception):
+    pass
+
+
+class Deadlock(Exception):
+    pass
+
+
+def _join(a, b):
+    out = dict(a)
+    for k, v in b.items():
+        if out.get(k, 0) < v:
+            out[k] = v
+    return out
+
+
+def mbarrier_counts(split):
+    """Expected arrivals per phase, as the kernel initialises them."""
+    c = {"QFULL": 1, "QEMPTY": 1, "OFINAL": 1, "OFREE": WARPS, "DRAIN0": 1, "DRAIN1": 1}
+    for d in (64, 128):
+        for s in range(max(KSTAGES.values())):
+            c[f"KFULL{s}"] = c[f"KEMPTY{s}"] = 1
+        for s in range(max(VSTAGES.values())):
+            c[f"VFULL{s}"] = c[f"VEMPTY{s}"] = 1
+    for b in range(2):
+        c[f"SFULL{b}"] = 1
+        if split:
+            c[f"PFULL{b}"] = c[f"PFULL{2 + b}"] = WARPS // 2
+            c[f"ODONE{b}"] = 1
+        else:
+            c[f"SREAD{b}"] = WARPS
+    if not split:
+        c["PFULL"] = WARPS
+        c["ODONE"] = 1
+    return c
+
+
+# ----------------------------------------------------------------- the roles
+# Actions a role yields:
+#   ("wait", bar, n)            wait for phase n of an mbarrier (n = -1: none yet)
+#   ("arrive", bar, n)          a thread's arrival, meant for phase n
+#   ("tma", bar, n, writes)     a TMA copy: arrive.expect_tx on phase n, the
+#                               bytes land later (complete_tx)
+#   ("mma", queue, reads, writes)   a tcgen05.mma issued into `queue`
+#   ("commit", queue, bar, n)   tcgen05.commit: arrives on phase n once every
+#                               MMA issued before it into `queue` is done
+#   ("nb_arrive", id, warps) / ("nb_sync", id, warps)   named barrier
+#   ("rd" | "wr", buffer)       a software access by the role
+
+
+def producer(items, D, mut):
+    KS, VS = KSTAGES[D], VSTAGES[D]
+    gk = gv = 0
+
+    def issue_v():
+        nonlocal gv
+        s = gv % VS
+        yield ("wait", f"VEMPTY{s}", gv // VS - 1)
+        yield ("tma", f"VFULL{s}", gv // VS, [f"V{s}"])
+        gv += 1
+
+    for k, n in enumerate(items):
+        yield ("wait", "QEMPTY", k - 1)
+        yield ("tma", "QFULL", k, ["Q"])
+        for _ in range(n):
+            s = gk % KS
+            yield ("wait", f"KEMPTY{s}", gk // KS - (2 if mut == "k_early" else 1))
+            yield ("tma", f"KFULL{s}", gk // KS, [f"K{s}"])
+            gk += 1
+            if gv <= gk - 3:
+                yield from issue_v()
+        while gv < gk:
+            yield from issue_v()
+    # drain: every copy lands before the CTA exits
+    if items:
+        yield ("wait", "QFULL", len(items) - 1)
+    for g in range(max(0, gk - KS), gk):
+        yield ("wait", f"KFULL{g % KS}", g // KS)
+    for g in range(max(0, gv - VS), gv):
+        yield ("wait", f"VFULL{g % VS}", g // VS)
+
+
+def score_issuer(items, D, split, mut):
+    KS = KSTAGES[D]
+    s_all = [f"S{{}}.{q}.{h}" for q in range(4) for h in range(2)]
+    g = 0
+
+    def signal_s_ready(gg):
+        yield ("wait", f"SFULL{gg & 1}", gg >> 1)
+        if split:
+            yield ("nb_arrive", 5 + gg % 3, 5)
+            yield ("nb_arrive", 8 + gg % 3, 5)
+        else:
+            yield ("nb_arrive", 5 + gg % 3, 9)
+
+    for k, n in enumerate(items):
+        for j in range(n):
+            b, s = g & 1, g % KS
+            if g >= 1:
+                yield from signal_s_ready(g - 1)
+            if j == 0:
+                yield ("wait", "QFULL", k)
+            yield ("wait", f"KFULL{s}", g // KS)
+            if g >= 2 and mut != "no_s_release":
+                yield ("wait", f"ODONE{b}" if split else f"SREAD{b}", (g - 2) >> 1)
+            yield ("mma", "S", ["Q", f"K{s}"], [x.format(b) for x in s_all])
+            yield ("commit", "S", f"KEMPTY{s}", g // KS)
+            yield ("commit", "S", f"SFULL{b}", g >> 1)
+            if j == n - 1:
+                yield ("commit", "S", "QEMPTY", k)
+            g += 1
+    if g >= 1:
+        yield from signal_s_ready(g - 1)
+    yield ("commit", "S", "DRAIN0", 0)
+    yield ("wait", "DRAIN0", 0)
+
+
+def pv_issuer(items, D, split, mut):
+    VS = VSTAGES[D]
+    g = 0
+    for k, n in enumerate(items):
+        if mut != "no_ofree":
+            yield ("wait", "OFREE", k - 1)
+        for j in range(n):
+            s, b = g % VS, g & 1
+            yield ("wait", f"VFULL{s}", g // VS)
+            if split:
+                for h in range(2):
+                    yield ("wait", f"PFULL{2 * (0 if mut == 'pv_one_half' else h) + b}", g >> 1)
+                    yield ("mma", "O", [f"S{b}.{q}.{h}" for q in range(4)] + [f"V{s}"],
+                           [f"O{h}.{q}.{c}" for q in range(4) for c in range(2)] + [f"L{h}.{q}" for q in range(4)])
+                yield ("commit", "O", f"VEMPTY{s}", g // VS)
+                yield ("commit", "O", f"ODONE{b}", g >> 1)
+            else:
+                yield ("wait", "PFULL", g)
+                yield ("mma", "O", [f"P.{q}.{h}" for q in range(4) for h in range(2)] + [f"V{s}"],
+                       [f"O.{q}.{h}" for q in range(4) for h in range(2)])
+                yield ("commit", "O", f"VEMPTY{s}", g // VS)
+                yield ("commit", "O", "ODONE", g)
+            if j == n - 1:
+                yield ("commit", "O", "OFINAL", k)
+            g += 1
+    yield ("commit", "O", "DRAIN1", 0)
+    yield ("wait", "DRAIN1", 0)
+
+
+def softmax_warp(w, items, D, split, need, mut):
+    """need[(key, g)]: the tile raises the row max enough to rescale; the key
+    is the lane quarter at d = 128 (both halves of a row decide alike) and the
+    warp in the split design (each half keeps its own reference max)."""
+    q, h = w & 3, w >> 2
+    g = 0
+    for k, n in enumerate(items):
+        for j in range(n):
+            b = g & 1
+            if split:
+                yield ("nb_sync", 5 + 3 * h + g % 3, 5)
+                yield ("rd", f"S{b}.{q}.{h}")
+                if j > 0 and need[(w, g)]:
+                    if mut != "no_rescale_wait":
+                        yield ("wait", f"ODONE{(g - 1) & 1}", (g - 1) >> 1)
+                    for r in (f"O{h}.{q}.0", f"O{h}.{q}.1", f"L{h}.{q}"):
+                        yield ("wr", r)
+                yield ("wr", f"S{b}.{q}.{h}")  # P over this half's scores
+                yield ("arrive", f"PFULL{2 * h + b}", g >> 1)
+            else:
+                yield ("nb_sync", 5 + g % 3, 9)
+                yield ("rd", f"S{b}.{q}.{h}")
+                yield ("arrive", f"SREAD{b}", g >> 1)
+                yield ("wr", f"MX.{q}.{b}.{h}")
+                if mut != "no_pair":
+                    yield ("nb_sync", 1 + q, 2)
+                yield ("rd", f"MX.{q}.{b}.{h ^ 1}")
+                waited = g == 0
+                if j > 0 and need[(q, g)]:
+                    if mut != "no_rescale_wait":
+                        yield ("wait", "ODONE", g - 1)
+                        waited = True
+                    yield ("wr", f"O.{q}.{h}")
+                if not waited and mut != "no_odone":
+                    yield ("wait", "ODONE", g - 1)
+                yield ("wr", f"P.{q}.{h}")
+                yield ("arrive", "PFULL", g)
+            g += 1
+        # epilogue
+        if mut != "no_ofinal":
+            yield ("wait", "OFINAL", k)
+        if split:
+            slot = 0 if mut == "one_xch_slot" else k & 1
+            yield ("rd", f"L{h}.{q}")
+            yield ("wr", f"X{slot}.{q}.{h}")
+            if mut != "no_pair":
+                yield ("nb_sync", 1 + q, 2)
+            yield ("rd", f"X{slot}.{q}.{h ^ 1}")
+            yield ("rd", f"O0.{q}.{h}")
+            yield ("rd", f"O1.{q}.{h}")
+        else:
+            yield ("wr", f"LX.{q}.{h}")
+            yield ("nb_sync", 1 + q, 2)
+            yield ("rd", f"LX.{q}.0")
+            yield ("rd", f"LX.{q}.1")
+            yield ("rd", f"O.{q}.{h}")
+        yield ("arrive", "OFREE", k)
+
+
+# ----------------------------------------------------------------- the model
+class MBar:
+    def __init__(self, count):
+        self.count = count
+        self.done = 0  # completed phases
+        self.arrived = 0
+        self.tx = 0
+        self.acc = {}
+        self.phase_vc = []
+
+
+class Model:
+    def __init__(self, split, seed):
+        self.rng = random.Random(seed)
+        self.bars = {name: MBar(c) for name, c in mbarrier_counts(split).items()}
+        self.nb = {}  # id -> [generation, count, arrived agents, accumulated clock]
+        self.nb_vc = {}  # (id, generation) -> clock
+        self.vc = {}  # agent -> vector clock
+        self.buf = {}  # buffer -> (last write (agent, epoch, who) or None, reads since it)
+        self.queues = {"S": [], "O": []}
+        self.queue_vc = {"S": {}, "O": {}}  # clock of the last MMA issued into the queue
+        self.inflight = []  # TMA copies: (bar, phase, clock)
+        self.blocked = {}  # agent -> ("mb", bar, n) | ("nb", id, generation)
+        self.n_ops = 0
+
+    # -- clocks
+    def _release(self, agent):
+        vc = dict(self.vc[agent])
+        self.vc[agent][agent] += 1
+        return vc
+
+    def _new_agent(self, name, vc):
+        vc = dict(vc)
+        vc[name] = 1
+        self.vc[name] = vc
+        return name
+
+    def _access(self, agent, buf, write):
+        vc = self.vc[agent]
+        last_w, reads = self.buf.get(buf, (None, []))
+        prior = ([last_w] if last_w else []) + (reads if write else [])
+        for a, e, _ in prior:
+            if a != agent and vc.get(a, 0) < e:
+                raise Violation(f"race on {buf}: {'write' if write else 'read'} by {agent} "
+                                f"is not ordered after an access by {a}")
+        me = (agent, vc[agent], "w" if write else "r")
+        self.buf[buf] = (me, []) if write else (last_w, reads + [me])
+
+    # -- mbarriers
+    def _arrive(self, bar_name, n, vc, tx=0, done_tx=False):
+        bar = self.bars[bar_name]
+        if bar.done != n:
+            raise Violation(f"arrival on {bar_name} meant for phase {n} lands in phase {bar.done}")
+        if done_tx:
+            bar.tx -= 1
+        else:
+            bar.arrived += 1
+            bar.tx += tx
+            if bar.arrived > bar.count:
+                raise Violation(f"{bar_name}: more arrivals than its count in phase {n}")
+        bar.acc = _join(bar.acc, vc)
+        if bar.arrived == bar.count and bar.tx == 0:
+            bar.phase_vc.append(bar.acc)
+            bar.done += 1
+            bar.arrived, bar.acc = 0, {}
+            for agent, st in self.blocked.items():
+                if st[0] == "mb" and st[1] == bar_name and bar.done > st[2] + 1:
+                    raise Violation(f"{agent} waits for phase {st[2]} of {bar_name} with parity {st[2] & 1}, "
+                                    f"but {bar.done} phases are complete: the parity aliases")
+
+    # -- named barriers
+    def _nb_arrive(self, agent, nid, warps):
+        st = self.nb.setdefault(nid, [0, warps, set(), {}])
+        if st[1] != warps:
+            raise Violation(f"named barrier {nid} used with {st[1]} and {warps} warps")
+        if agent in st[2]:
+            raise Violation(f"overrun: {agent} arrives twice in generation {st[0]} of named barrier {nid}")
+        st[2].add(agent)
+        st[3] = _join(st[3], self._release(agent))
+        gen = st[0]
+        if len(st[2]) == warps:
+            self.nb_vc[(nid, gen)] = st[3]
+            st[0], st[2], st[3] = gen + 1, set(), {}
+        return gen
+
+    # -- one action of a role
+    def _do(self, agent, act):
+        kind = act[0]
+        if kind == "wait":
+            _, bar_name, n = act
+            bar = self.bars[bar_name]
+            if bar.done < n:
+                raise Violation(f"{agent} waits for phase {n} of {bar_name} with only {bar.done} complete: "
+                                "a parity wait would return on an earlier phase")
+            self.blocked[agent] = ("mb", bar_name, n)
+        elif kind == "arrive":
+            self._arrive(act[1], act[2], self._release(agent))
+        elif kind == "tma":
+            _, bar_name, n, writes = act
+            self.n_ops += 1
+            op = self._new_agent(f"tma{self.n_ops}", self._release(agent))
+            for w in writes:
+                self._access(op, w, True)
+            self._arrive(bar_name, n, self.vc[agent], tx=1)
+            self.inflight.append((bar_name, n, self.vc[op]))
+        elif kind == "mma":
+            _, qn, reads, writes = act
+            self.n_ops += 1
+            op = self._new_agent(f"mma{qn}{self.n_ops}", _join(self._release(agent), self.queue_vc[qn]))
+            for r in reads:
+                self._access(op, r, False)
+            for w in writes:
+                self._access(op, w, True)
+            self.queue_vc[qn] = self.vc[op]
+            self.queues[qn].append(None)
+        elif kind == "commit":
+            _, qn, bar_name, n = act
+            self.queues[qn].append((bar_name, n, self.queue_vc[qn]))
+        elif kind in ("nb_arrive", "nb_sync"):
+            gen = self._nb_arrive(agent, act[1], act[2])
+            if kind == "nb_sync":
+                self.blocked[agent] = ("nb", act[1], gen)
+        elif kind in ("rd", "wr"):
+            self._access(agent, act[1], kind == "wr")
+        else:
+            raise AssertionError(act)
+
+    def run(self, roles, max_steps=200000):
+        for name in roles:
+            self.vc[name] = {name: 1}
+        live = dict(roles)
+        for _ in range(max_steps):
+            choices = []
+            for name in live:
+                st = self.blocked.get(name)
+                if st is None:
+                    choices.append(("role", name))
+                elif st[0] == "mb" and self.bars[st[1]].done >= st[2] + 1:
+                    choices.append(("role", name))
+                elif st[0] == "nb" and self.nb[st[1]][0] > st[2]:
+                    choices.append(("role", name))
+            choices += [("tc", qn) for qn, qu in self.queues.items() if qu]
+            choices += [("tma", i) for i in range(len(self.inflight))]
+            if not choices:
+                if live:
+                    raise Deadlock({n: self.blocked.get(n) for n in live})
+                break
+            kind, x = self.rng.choice(choices)
+            if kind == "tc":
+                entry = self.queues[x].pop(0)
+                if entry is not None:  # a commit: every MMA before it is done
+                    self._arrive(entry[0], entry[1], entry[2])
+            elif kind == "tma":
+                bar_name, n, vc = self.inflight.pop(x)
+                self._arrive(bar_name, n, vc, done_tx=True)
+            else:
+                st = self.blocked.pop(x, None)
+                if st is not None and st[0] == "mb" and st[2] >= 0:
+                    self.vc[x] = _join(self.vc[x], self.bars[st[1]].phase_vc[st[2]])
+                elif st is not None and st[0] == "nb":
+                    self.vc[x] = _join(self.vc[x], self.nb_vc[(st[1], st[2])])
+                try:
+                    act = next(live[x])
+                except StopIteration:
+                    del live[x]
+                    continue
+                self._do(x, act)
+        else:
+            raise AssertionError("step limit")
+        for nid, st in self.nb.items():
+            if st[2]:
+                raise Violation(f"named barrier {nid} ends with an incomplete generation")
+        for name, bar in self.bars.items():
+            if bar.arrived or bar.tx:
+                raise Violation(f"mbarrier {name} ends with arrivals pending")
+
+
+def simulate(D, seed, items=None, mut=None):
+    rng = random.Random(seed * 7919 + D)
+    if items is None:
+        items = [rng.randint(1, 5) for _ in range(rng.randint(1, 4))]
+    split = D == 64
+    tiles = sum(items)
+    p_need = rng.choice([0.0, 0.3, 1.0])
+    keys = range(WARPS) if split else range(4)
+    need = {(key, g): rng.random() < p_need for key in keys for g in range(tiles)}
+    roles = {
+        "producer": producer(items, D, mut),
+        "score": score_issuer(items, D, split, mut),
+        "pv": pv_issuer(items, D, split, mut),
+    }
+    for w in range(WARPS):
+        roles[f"softmax{w}"] = softmax_warp(w, items, D, split, need, mut)
+    Model(split, seed).run(roles)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_forward_pipeline_is_race_free_and_parity_safe(D):
+    for seed in range(120):
+        simulate(D, seed)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("items", [[1], [1, 1, 1, 1, 1], [7], [2, 1, 3], [1, 6, 1]])
+def test_forward_pipeline_item_shapes(D, items):
+    """Single-tile items (the Q, O-free and O-final barriers turn over every
+    tile), one long item (the K and V rings wrap several times) and mixes."""
+    for seed in range(40):
+        simulate(D, seed, items=items)
+
+
+MUTANTS = [
+    # (designs, mistake, what it breaks)
+    ((128, 64), "no_s_release", "the score issuer reuses an S buffer without waiting for its readers"),
+    ((128,), "no_odone", "P is written before the previous P.V has read the P buffer"),
+    ((128, 64), "no_rescale_wait", "O is rescaled while the previous P.V may still add to it"),
+    ((128, 64), "no_pair", "the partner's row max (d = 128) or epilogue values (split) are read "
+                           "without the pair barrier"),
+    ((64,), "pv_one_half", "a half's P.V waits for the other half's P only"),
+    ((64,), "no_ofree", "the next item's first P.V overwrites O before the other half's epilogue read it"),
+    ((128, 64), "no_ofinal", "the epilogue reads O before the item's last P.V is done"),
+    ((128, 64), "k_early", "the producer refills a K stage one phase too early"),
+]
+
+
+@pytest.mark.parametrize("designs, mut, what", MUTANTS, ids=[m[1] for m in MUTANTS])
+def test_planted_protocol_mistakes_are_caught(designs, mut, what):
+    for D in designs:
+        caught = None
+        for seed in range(400):
+            try:
+                simulate(D, seed, mut=mut)
+            except (Violation, Deadlock) as e:
+                caught = e
+                break
+        assert caught is not None, f"d = {D}: not caught: {what}"
+
+
+def test_redundant_orderings():
+    """Two orderings the kernel spells out are implied by others:
+    - at d = 128 the P.V issuer's wait for "O read out": the first P.V of the
+      next item waits for P-full, and each of the eight softmax warps arrives
+      on it only after its own epilogue has read O (in the split design it is
+      needed: a half's P.V waits for that half's four warps only, while the
+      other half's epilogue reads both accumulators);
+    - in the split design, one epilogue exchange slot instead of one per item
+      parity: the partner reads the slot before it arrives on "O read out",
+      and the next write follows "O final" of the next item, which the P.V
+      issuer commits only after waiting for "O read out"."""
+    for seed in range(150):
+        simulate(128, seed, mut="no_ofree")
+        simulate(64, seed, mut="one_xch_slot")
