@@ -12,8 +12,8 @@ checks:
   stages in shared memory; the S, P and O regions of TMEM per lane quarter
   and half row; the row-max, row-sum and epilogue exchange slots) are ordered
   by happens-before.  Vector clocks travel through mbarrier phases, named
-  barrier generations, MMA commits and TMA completions; MMAs issued by one
-  thread execute in order;
+  barrier generations, MMA commits and TMA completions (the model and its
+  rules are in _pipeline_model.py);
 * parity safety: a wait for phase n of an mbarrier (parity n mod 2) starts
   with at least n phases complete and returns before phase n + 1 completes,
   so the parity cannot alias;
@@ -32,35 +32,20 @@ import random
 
 import pytest
 
+from _pipeline_model import Deadlock, Model, Violation
+
 KSTAGES = {128: 3, 64: 4}
 VSTAGES = {128: 2, 64: 4}
 WARPS = 8  # softmax warps: warp w serves lane quarter w % 4, half row w // 4
 
 
-class Violation(Exception):
-    pass
-
-
-class Deadlock(Exception):
-    pass
-
-
-def _join(a, b):
-    out = dict(a)
-    for k, v in b.items():
-        if out.get(k, 0) < v:
-            out[k] = v
-    return out
-
-
 def mbarrier_counts(split):
     """Expected arrivals per phase, as the kernel initialises them."""
     c = {"QFULL": 1, "QEMPTY": 1, "OFINAL": 1, "OFREE": WARPS, "DRAIN0": 1, "DRAIN1": 1}
-    for d in (64, 128):
-        for s in range(max(KSTAGES.values())):
-            c[f"KFULL{s}"] = c[f"KEMPTY{s}"] = 1
-        for s in range(max(VSTAGES.values())):
-            c[f"VFULL{s}"] = c[f"VEMPTY{s}"] = 1
+    for s in range(max(KSTAGES.values())):
+        c[f"KFULL{s}"] = c[f"KEMPTY{s}"] = 1
+    for s in range(max(VSTAGES.values())):
+        c[f"VFULL{s}"] = c[f"VEMPTY{s}"] = 1
     for b in range(2):
         c[f"SFULL{b}"] = 1
         if split:
@@ -75,16 +60,7 @@ def mbarrier_counts(split):
 
 
 # ----------------------------------------------------------------- the roles
-# Actions a role yields:
-#   ("wait", bar, n)            wait for phase n of an mbarrier (n = -1: none yet)
-#   ("arrive", bar, n)          a thread's arrival, meant for phase n
-#   ("tma", bar, n, writes)     a TMA copy: arrive.expect_tx on phase n, the
-#                               bytes land later (complete_tx)
-#   ("mma", queue, reads, writes)   a tcgen05.mma issued into `queue`
-#   ("commit", queue, bar, n)   tcgen05.commit: arrives on phase n once every
-#                               MMA issued before it into `queue` is done
-#   ("nb_arrive", id, warps) / ("nb_sync", id, warps)   named barrier
-#   ("rd" | "wr", buffer)       a software access by the role
+# The roles yield the actions listed in _pipeline_model.
 
 
 def producer(items, D, mut):
@@ -142,7 +118,7 @@ def score_issuer(items, D, split, mut):
             yield ("wait", f"KFULL{s}", g // KS)
             if g >= 2 and mut != "no_s_release":
                 yield ("wait", f"ODONE{b}" if split else f"SREAD{b}", (g - 2) >> 1)
-            yield ("mma", "S", ["Q", f"K{s}"], [x.format(b) for x in s_all])
+            yield ("mma", "S", ["Q", f"K{s}"], [x.format(b) for x in s_all], [])
             yield ("commit", "S", f"KEMPTY{s}", g // KS)
             yield ("commit", "S", f"SFULL{b}", g >> 1)
             if j == n - 1:
@@ -166,13 +142,13 @@ def pv_issuer(items, D, split, mut):
             if split:
                 for h in range(2):
                     yield ("wait", f"PFULL{2 * (0 if mut == 'pv_one_half' else h) + b}", g >> 1)
-                    yield ("mma", "O", [f"S{b}.{q}.{h}" for q in range(4)] + [f"V{s}"],
+                    yield ("mma", "O", [f"S{b}.{q}.{h}" for q in range(4)] + [f"V{s}"], [],
                            [f"O{h}.{q}.{c}" for q in range(4) for c in range(2)] + [f"L{h}.{q}" for q in range(4)])
                 yield ("commit", "O", f"VEMPTY{s}", g // VS)
                 yield ("commit", "O", f"ODONE{b}", g >> 1)
             else:
                 yield ("wait", "PFULL", g)
-                yield ("mma", "O", [f"P.{q}.{h}" for q in range(4) for h in range(2)] + [f"V{s}"],
+                yield ("mma", "O", [f"P.{q}.{h}" for q in range(4) for h in range(2)] + [f"V{s}"], [],
                        [f"O.{q}.{h}" for q in range(4) for h in range(2)])
                 yield ("commit", "O", f"VEMPTY{s}", g // VS)
                 yield ("commit", "O", "ODONE", g)
@@ -242,183 +218,6 @@ def softmax_warp(w, items, D, split, need, mut):
         yield ("arrive", "OFREE", k)
 
 
-# ----------------------------------------------------------------- the model
-class MBar:
-    def __init__(self, count):
-        self.count = count
-        self.done = 0  # completed phases
-        self.arrived = 0
-        self.tx = 0
-        self.acc = {}
-        self.phase_vc = []
-
-
-class Model:
-    def __init__(self, split, seed):
-        self.rng = random.Random(seed)
-        self.bars = {name: MBar(c) for name, c in mbarrier_counts(split).items()}
-        self.nb = {}  # id -> [generation, count, arrived agents, accumulated clock]
-        self.nb_vc = {}  # (id, generation) -> clock
-        self.vc = {}  # agent -> vector clock
-        self.buf = {}  # buffer -> (last write (agent, epoch, who) or None, reads since it)
-        self.queues = {"S": [], "O": []}
-        self.queue_vc = {"S": {}, "O": {}}  # clock of the last MMA issued into the queue
-        self.inflight = []  # TMA copies: (bar, phase, clock)
-        self.blocked = {}  # agent -> ("mb", bar, n) | ("nb", id, generation)
-        self.n_ops = 0
-
-    # -- clocks
-    def _release(self, agent):
-        vc = dict(self.vc[agent])
-        self.vc[agent][agent] += 1
-        return vc
-
-    def _new_agent(self, name, vc):
-        vc = dict(vc)
-        vc[name] = 1
-        self.vc[name] = vc
-        return name
-
-    def _access(self, agent, buf, write):
-        vc = self.vc[agent]
-        last_w, reads = self.buf.get(buf, (None, []))
-        prior = ([last_w] if last_w else []) + (reads if write else [])
-        for a, e, _ in prior:
-            if a != agent and vc.get(a, 0) < e:
-                raise Violation(f"race on {buf}: {'write' if write else 'read'} by {agent} "
-                                f"is not ordered after an access by {a}")
-        me = (agent, vc[agent], "w" if write else "r")
-        self.buf[buf] = (me, []) if write else (last_w, reads + [me])
-
-    # -- mbarriers
-    def _arrive(self, bar_name, n, vc, tx=0, done_tx=False):
-        bar = self.bars[bar_name]
-        if bar.done != n:
-            raise Violation(f"arrival on {bar_name} meant for phase {n} lands in phase {bar.done}")
-        if done_tx:
-            bar.tx -= 1
-        else:
-            bar.arrived += 1
-            bar.tx += tx
-            if bar.arrived > bar.count:
-                raise Violation(f"{bar_name}: more arrivals than its count in phase {n}")
-        bar.acc = _join(bar.acc, vc)
-        if bar.arrived == bar.count and bar.tx == 0:
-            bar.phase_vc.append(bar.acc)
-            bar.done += 1
-            bar.arrived, bar.acc = 0, {}
-            for agent, st in self.blocked.items():
-                if st[0] == "mb" and st[1] == bar_name and bar.done > st[2] + 1:
-                    raise Violation(f"{agent} waits for phase {st[2]} of {bar_name} with parity {st[2] & 1}, "
-                                    f"but {bar.done} phases are complete: the parity aliases")
-
-    # -- named barriers
-    def _nb_arrive(self, agent, nid, warps):
-        st = self.nb.setdefault(nid, [0, warps, set(), {}])
-        if st[1] != warps:
-            raise Violation(f"named barrier {nid} used with {st[1]} and {warps} warps")
-        if agent in st[2]:
-            raise Violation(f"overrun: {agent} arrives twice in generation {st[0]} of named barrier {nid}")
-        st[2].add(agent)
-        st[3] = _join(st[3], self._release(agent))
-        gen = st[0]
-        if len(st[2]) == warps:
-            self.nb_vc[(nid, gen)] = st[3]
-            st[0], st[2], st[3] = gen + 1, set(), {}
-        return gen
-
-    # -- one action of a role
-    def _do(self, agent, act):
-        kind = act[0]
-        if kind == "wait":
-            _, bar_name, n = act
-            bar = self.bars[bar_name]
-            if bar.done < n:
-                raise Violation(f"{agent} waits for phase {n} of {bar_name} with only {bar.done} complete: "
-                                "a parity wait would return on an earlier phase")
-            self.blocked[agent] = ("mb", bar_name, n)
-        elif kind == "arrive":
-            self._arrive(act[1], act[2], self._release(agent))
-        elif kind == "tma":
-            _, bar_name, n, writes = act
-            self.n_ops += 1
-            op = self._new_agent(f"tma{self.n_ops}", self._release(agent))
-            for w in writes:
-                self._access(op, w, True)
-            self._arrive(bar_name, n, self.vc[agent], tx=1)
-            self.inflight.append((bar_name, n, self.vc[op]))
-        elif kind == "mma":
-            _, qn, reads, writes = act
-            self.n_ops += 1
-            op = self._new_agent(f"mma{qn}{self.n_ops}", _join(self._release(agent), self.queue_vc[qn]))
-            for r in reads:
-                self._access(op, r, False)
-            for w in writes:
-                self._access(op, w, True)
-            self.queue_vc[qn] = self.vc[op]
-            self.queues[qn].append(None)
-        elif kind == "commit":
-            _, qn, bar_name, n = act
-            self.queues[qn].append((bar_name, n, self.queue_vc[qn]))
-        elif kind in ("nb_arrive", "nb_sync"):
-            gen = self._nb_arrive(agent, act[1], act[2])
-            if kind == "nb_sync":
-                self.blocked[agent] = ("nb", act[1], gen)
-        elif kind in ("rd", "wr"):
-            self._access(agent, act[1], kind == "wr")
-        else:
-            raise AssertionError(act)
-
-    def run(self, roles, max_steps=200000):
-        for name in roles:
-            self.vc[name] = {name: 1}
-        live = dict(roles)
-        for _ in range(max_steps):
-            choices = []
-            for name in live:
-                st = self.blocked.get(name)
-                if st is None:
-                    choices.append(("role", name))
-                elif st[0] == "mb" and self.bars[st[1]].done >= st[2] + 1:
-                    choices.append(("role", name))
-                elif st[0] == "nb" and self.nb[st[1]][0] > st[2]:
-                    choices.append(("role", name))
-            choices += [("tc", qn) for qn, qu in self.queues.items() if qu]
-            choices += [("tma", i) for i in range(len(self.inflight))]
-            if not choices:
-                if live:
-                    raise Deadlock({n: self.blocked.get(n) for n in live})
-                break
-            kind, x = self.rng.choice(choices)
-            if kind == "tc":
-                entry = self.queues[x].pop(0)
-                if entry is not None:  # a commit: every MMA before it is done
-                    self._arrive(entry[0], entry[1], entry[2])
-            elif kind == "tma":
-                bar_name, n, vc = self.inflight.pop(x)
-                self._arrive(bar_name, n, vc, done_tx=True)
-            else:
-                st = self.blocked.pop(x, None)
-                if st is not None and st[0] == "mb" and st[2] >= 0:
-                    self.vc[x] = _join(self.vc[x], self.bars[st[1]].phase_vc[st[2]])
-                elif st is not None and st[0] == "nb":
-                    self.vc[x] = _join(self.vc[x], self.nb_vc[(st[1], st[2])])
-                try:
-                    act = next(live[x])
-                except StopIteration:
-                    del live[x]
-                    continue
-                self._do(x, act)
-        else:
-            raise AssertionError("step limit")
-        for nid, st in self.nb.items():
-            if st[2]:
-                raise Violation(f"named barrier {nid} ends with an incomplete generation")
-        for name, bar in self.bars.items():
-            if bar.arrived or bar.tx:
-                raise Violation(f"mbarrier {name} ends with arrivals pending")
-
-
 def simulate(D, seed, items=None, mut=None):
     rng = random.Random(seed * 7919 + D)
     if items is None:
@@ -435,7 +234,7 @@ def simulate(D, seed, items=None, mut=None):
     }
     for w in range(WARPS):
         roles[f"softmax{w}"] = softmax_warp(w, items, D, split, need, mut)
-    Model(split, seed).run(roles)
+    Model(mbarrier_counts(split), seed).run(roles)
 
 
 @pytest.mark.parametrize("D", [128, 64])
