@@ -4,7 +4,9 @@ A kernel's roles are written as Python generators that yield the barrier
 operations and buffer accesses of the kernel, in its order.  `Model.run`
 executes them under one random interleaving, with random completion times for
 the asynchronous work (TMA copies, tcgen05 MMAs and commits, bulk reduce
-copies), and carries vector clocks through every synchronisation:
+copies; each run draws how fast that work is against the threads, from much
+slower to much faster), and carries vector clocks through every
+synchronisation:
 
 * an mbarrier phase releases the join of its arrivals (a TMA copy's arrival
   carries the copy, a commit carries every MMA its issuer issued before it);
@@ -74,6 +76,8 @@ class _MBar:
 class Model:
     def __init__(self, counts, seed, queues=("S", "O")):
         self.rng = random.Random(seed)
+        # weight of an asynchronous completion against a thread's step
+        self.engine_weight = self.rng.choice([0.05, 0.3, 1.0, 3.0, 20.0])
         self.bars = {name: _MBar(c) for name, c in counts.items()}
         self.nb = {}  # id -> [generation, warps, arrived agents, accumulated clock]
         self.nb_vc = {}  # (id, generation) -> clock
@@ -221,15 +225,16 @@ class Model:
             self.vc[name] = {name: 1}
         live = dict(roles)
         for _ in range(max_steps):
-            choices = [("role", n) for n in live if self._runnable(n)]
-            choices += [("tc", qn) for qn, qu in self.queues.items() if qu]
-            choices += [("tma", i) for i in range(len(self.inflight))]
-            choices += [("bulk", i) for i in range(len(self.bulk_pending))]
-            if not choices:
+            roles_ready = [("role", n) for n in live if self._runnable(n)]
+            engine = [("tc", qn) for qn, qu in self.queues.items() if qu]
+            engine += [("tma", i) for i in range(len(self.inflight))]
+            engine += [("bulk", i) for i in range(len(self.bulk_pending))]
+            if not roles_ready and not engine:
                 if live:
                     raise Deadlock({n: self.blocked.get(n) for n in live})
                 break
-            kind, x = self.rng.choice(choices)
+            kind, x = self.rng.choices(roles_ready + engine,
+                                       [1.0] * len(roles_ready) + [self.engine_weight] * len(engine))[0]
             if kind == "tc":
                 entry = self.queues[x].pop(0)
                 if entry is not None:  # a commit: every MMA before it is done
