@@ -1,7 +1,7 @@
 """Oracle for softmax attention: plain fp64 CPU code, TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg may import this package.  The product path (``io_aware_attention_gb300``)
+and reference legs may import this package.  The product path (``io_aware_attention_gb300``)
 never imports it and shares no code with it.
 
 The arithmetic lives in ``attn_ref.c`` (compiled with gcc into
