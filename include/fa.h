@@ -248,6 +248,17 @@ fa_status fa_bias_gelu_dropout(const void *x, const void *bias, const uint32_t *
 fa_status fa_check_device_status(fa_stream_t stream, uint32_t *where);
 
 /*
+ * fa_get_device_status — fa_check_device_status without the wait code:
+ * synchronises `stream`, reads and clears the device status word of the
+ * current device, and returns FA_OK, FA_ERR_TIMEOUT (a kernel gave up a
+ * bounded wait; its outputs are incomplete) or FA_ERR_CUDA.  The deferred
+ * report of errors that happen inside a launch ("Writing and Benchmarking
+ * Custom Kernels" §10.2.1: kernel errors surface only at a later
+ * synchronisation).
+ */
+fa_status fa_get_device_status(fa_stream_t stream);
+
+/*
  * fa_set_wait_limit_ns — upper bound, in nanoseconds, on any single pipeline
  * wait inside the kernels launched after this call (default 1e9 = 1 s; 0
  * restores the default).  Affects only how quickly a stuck kernel gives up.

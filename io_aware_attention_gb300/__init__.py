@@ -36,12 +36,12 @@ import os
 
 from . import _build
 
-__all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "bias_gelu_dropout", "decode", "decode_into", "decode_workspace_bytes", "check_device_status",
+__all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "bias_gelu_dropout", "decode", "decode_into", "decode_workspace_bytes", "check_device_status", "get_device_status",
            "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
-EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bias_gelu_dropout", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status",
+EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bias_gelu_dropout", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status", "fa_get_device_status",
            "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
 
 
@@ -90,6 +90,8 @@ def library():
     lib.fa_decode_static.restype = ctypes.c_int
     lib.fa_check_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.fa_check_device_status.restype = ctypes.c_int
+    lib.fa_get_device_status.argtypes = [vp]
+    lib.fa_get_device_status.restype = ctypes.c_int
     lib.fa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.fa_set_wait_limit_ns.restype = ctypes.c_int
     lib.fa_debug_skip_k_tile.argtypes = [ctypes.c_int]
@@ -333,6 +335,15 @@ def check_device_status(stream=None) -> int:
     rc = library().fa_check_device_status(_stream_handle(stream), ctypes.byref(where))
     if rc == 3:
         raise FaError(rc, "fa_check_device_status")
+    return rc
+
+
+def get_device_status(stream=None) -> int:
+    """fa_get_device_status: synchronises the stream and returns the device
+    status (0 = ok, 4 = a wait timed out); raises FaError on a CUDA error."""
+    rc = library().fa_get_device_status(_stream_handle(stream))
+    if rc == 3:
+        raise FaError(rc, "fa_get_device_status")
     return rc
 
 

@@ -70,6 +70,19 @@ def test_bad_arguments_are_rejected(lib, kw, status):
     assert call(lib, **kw) == status
 
 
+def test_device_status_without_a_gpu_is_a_cuda_error(lib):
+    """Both status calls report FA_ERR_CUDA, not a crash, when no device can be
+    read (this container has none; on a GPU machine they are exercised by
+    tests/test_fa_timeout.py)."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    where = ctypes.c_uint32(7)
+    assert lib.fa_check_device_status(None, ctypes.byref(where)) == 3
+    assert lib.fa_get_device_status(None) == 3
+
+
 def test_wait_limit_setter(lib):
     assert lib.fa_set_wait_limit_ns(5_000_000) == 0
     assert lib.fa_set_wait_limit_ns(0) == 0  # back to the default

@@ -69,3 +69,20 @@ def test_bwd_wait_timeout_is_reported_and_recoverable(causal, tile):
     torch.cuda.synchronize()
     assert fa.check_device_status() == 0
     check_heads(q, k, v, do, causal, scale, dq, dk, dv, range(B * H), "after timeout")
+
+
+def test_get_device_status_reports_and_clears():
+    """fa_get_device_status, the short form: FA_ERR_TIMEOUT once, then FA_OK."""
+    q, k, v = (t.cuda() for t in make_random_qkv(1, 2, 640, 128, seed=24))
+    assert fa.get_device_status() == 0
+    fa.set_wait_limit_ns(20_000_000)  # 20 ms
+    fa.debug_skip_k_tile(1)
+    try:
+        fa.fwd(q, k, v, causal=False)
+        assert fa.get_device_status() == 4  # FA_ERR_TIMEOUT
+    finally:
+        fa.debug_skip_k_tile(-1)
+        fa.set_wait_limit_ns(0)
+    assert fa.get_device_status() == 0
+    fa.fwd(q, k, v, causal=False)
+    assert fa.get_device_status() == 0
