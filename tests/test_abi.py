@@ -70,6 +70,24 @@ def test_bad_arguments_are_rejected(lib, kw, status):
     assert call(lib, **kw) == status
 
 
+def test_plain_c_client(lib, tmp_path):
+    """The boundary is a C ABI: a C program built with gcc against fa.h alone
+    links the library and gets the answers the header promises."""
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    exe = str(tmp_path / "abi_client")
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "abi_client.c")
+    libdir = os.path.dirname(_build.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", _build.INCLUDE, src, "-o", exe, "-L", libdir,
+                    "-l:" + os.path.basename(_build.LIB_PATH), "-Wl,-rpath," + libdir], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert "FAIL" not in r.stdout and r.stdout.count("ok ") == 9
+
+
 def test_device_status_without_a_gpu_is_a_cuda_error(lib):
     """Both status calls report FA_ERR_CUDA, not a crash, when no device can be
     read (this container has none; on a GPU machine they are exercised by
