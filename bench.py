@@ -19,9 +19,17 @@ causal mask.
   with two device buffer sets, so one step's copies overlap its neighbours'
   compute (pipelined_e2e).
 * roofline: the attention kernel is tensor-core bound; achieved = algorithmic
-  FLOPs per launch / mean launch time, against the measured bf16 GEMM peak.
+  FLOPs per launch / mean launch time, against the measured bf16 GEMM peak
+  (frac), the measured sustained peak and NVIDIA's datasheet dense figure;
+  beside it the exponential unit's bound (one ex2 per score).
+* blocks beside the headline (default run): non_causal (the other half of
+  the metric, B=8 H=32 N=4096 d=128), sustained (the headline launch
+  repeated for a seconds-long region under the power cap) and one block per
+  other configuration, each with its own clocks, launch spread and roofline;
+  the small configuration also reports the host cost of a call.
 * cpu_baseline: the fp64 CPU oracle timed on the host cores over a bounded
-  sample of rows of the same workload (rank 0 only).
+  sample of rows of the same workload (rank 0 only), with all threads and
+  with one, and the full tensor's time extrapolated from those rates.
 * --impl reference: the oracle alone (the reference arm: the pages ship no
   runnable code), each step a bounded sample of rows.
 * --workload ew_*: the fused elementwise chain (bias + GELU + dropout) of
@@ -84,6 +92,18 @@ MEASURED_TRAFFIC = {
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# NVIDIA's published dense BF16 tensor figure for one GB300 GPU: its HGX B300
+# table gives 36 PFLOPS of FP16/BF16 for 8 GPUs with 2:4 sparsity, i.e. 4.5
+# sparse and 2.25 dense PFLOPS per GPU.  A second denominator beside the
+# measured cuBLAS peak.
+DATASHEET_BF16_TFLOPS = 2250.0
+DATASHEET_SOURCE = ("NVIDIA HGX B300 specification (nvidia.com/en-us/data-center/hgx/): 36 PFLOPS FP16/BF16 "
+                    "for 8 GPUs, with sparsity; dense per GPU = 36 / 8 / 2")
+# The special-function unit's exponential: one ex2.approx.f32 warp
+# instruction issues every 4.2 cycles per SM sub-partition (a probe of
+# back-to-back independent ex2 on this GPU), i.e. 4 x 32 / 4.2 = 30.5
+# exponentials per cycle per SM.  The kernel evaluates one per score.
+EX2_CYCLES_PER_WARP_INSTR = 4.2
 
 
 def parse_args(argv=None):
@@ -99,6 +119,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time budget")
+    ap.add_argument("--no-blocks", action="store_true",
+                    help="headline only: skip the non-causal, sustained and per-configuration blocks")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of the sustained block's timed region")
     return ap.parse_args(argv)
 
 
@@ -299,6 +323,156 @@ class ClockSampler:
                 "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def timed_region(step, n, stream, gpu_index, barrier, label):
+    """Milliseconds of n calls of step() on `stream` (CUDA events), between a
+    barrier and a synchronisation on both sides, with nvidia-smi clock
+    samples taken while they run (gpu_index None: no sampling) and an NVTX
+    range around the launches."""
+    import torch
+
+    sampler = ClockSampler(gpu_index) if gpu_index is not None else None
+    if sampler:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push(label)
+    ev0.record(stream)
+    for _ in range(n):
+        step()
+    ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    return ev0.elapsed_time(ev1), clocks
+
+
+def single_launch_stats(step, stream, n=30):
+    """Median, standard deviation and minimum of n single launches, each
+    bracketed by its own events."""
+    import torch
+
+    pairs = []
+    for _ in range(n):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in pairs]
+    return {"n": len(ms), "median_ms": round(statistics.median(ms), 5), "stdev_ms": round(statistics.stdev(ms), 5),
+            "min_ms": round(min(ms), 5)}
+
+
+def mufu_bound(w, ms_per_step: float, sm_mhz, sms: int):
+    """Time bound of the exponentials: one ex2 per score the method computes
+    (B*H*N^2, half of it under the causal mask), at the special-function
+    unit's measured rate and the median SM clock of the timed region."""
+    if not sm_mhz:
+        return None
+    scores = w.B * w.H * w.N * w.N * (0.5 if w.causal else 1.0)
+    rate = sms * 4 * 32 / EX2_CYCLES_PER_WARP_INSTR * sm_mhz * 1e6
+    bound_ms = scores / rate * 1e3
+    return {"ex2_per_s": round(rate / 1e12, 3), "unit": "Tex2/s", "scores_per_launch": scores,
+            "bound_ms": round(bound_ms, 5), "frac": round(bound_ms / ms_per_step, 4), "sm_mhz": sm_mhz,
+            "rate": f"{sms} SMs x 4 x 32 / {EX2_CYCLES_PER_WARP_INSTR} ex2 per cycle at the median SM clock"}
+
+
+def tensor_roofline(w, flops: float, ms_per_step: float, peaks, peak_src, clocks, sms: int, kernel: str):
+    """The forward's roofline entry: algorithmic FLOPs per launch over the
+    launch time, against the measured bf16 burst peak (the denominator of
+    frac), the sustained peak and the datasheet figure; and the exponential
+    unit's bound, with the tighter of the two bounds named."""
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    tensor_ms = flops / (peak * 1e12) * 1e3
+    mufu = mufu_bound(w, ms_per_step, clocks.get("sm_mhz") if clocks else None, sms)
+    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
+            "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+            "frac_of_datasheet": round(achieved / DATASHEET_BF16_TFLOPS, 4),
+            "datasheet_tflops": DATASHEET_BF16_TFLOPS, "kernel": kernel, "alg_flops_per_launch": flops,
+            "tensor_bound_ms": round(tensor_ms, 5), "mufu": mufu}
+    if mufu:
+        roof["binding"] = "tensor" if tensor_ms >= mufu["bound_ms"] else "mufu"
+        roof["frac_of_binding"] = round(max(tensor_ms, mufu["bound_ms"]) / ms_per_step, 4)
+    return roof
+
+
+def fwd_kernel_name(w) -> str:
+    D = 64 if w.d <= 64 else 128
+    return f"fa::fa_fwd_kernel<{D},{str(w.causal).lower()},{str(w.d != D).lower()},*>"
+
+
+def fwd_block(fa, w, dev, stream, peaks, peak_src, sms, rank, barrier, min_seconds=0.25, min_steps=20,
+              host_cost=False):
+    """One workload of the default run, beside the headline: its own inputs,
+    timed region (at least min_seconds and min_steps launches), clocks, launch
+    spread and roofline."""
+    import torch
+
+    from io_aware_attention_gb300 import iomodel
+    from io_aware_attention_gb300.workloads import make_qkv
+
+    flops = iomodel.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    q, k, v = (t.to(dev) for t in make_qkv(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+
+    def step():
+        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    probe_ms, _ = timed_region(step, 5, stream, None, lambda: None, "probe")
+    n = max(min_steps, int(min_seconds / max(probe_ms / 5 * 1e-3, 1e-7)) + 1)
+    ms, clocks = timed_region(step, n, stream, torch.cuda.current_device() if rank == 0 else None, barrier,
+                              f"fa_fwd {w.name}")
+    if fa.check_device_status() != 0:
+        raise RuntimeError(f"kernel reported a timed-out wait ({w.name})")
+    ms_per_step = max_over_ranks(ms, dev) / n
+    blk = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+           "steps": n, "ms_per_step": round(ms_per_step, 5), "value": round(flops / (ms_per_step * 1e-3) / 1e12, 2),
+           "unit": "TFLOP/s", "timed_s": round(ms / 1e3, 3),
+           "roofline": tensor_roofline(w, flops, ms_per_step, peaks, peak_src, clocks, sms, fwd_kernel_name(w)),
+           "launch_stats": single_launch_stats(step, stream), "clocks": clocks}
+    if host_cost:
+        blk["host_us_per_call"] = host_call_cost(fa, q, k, v, o, lse, w, stream)
+    del q, k, v, o, lse
+    return blk
+
+
+def host_call_cost(fa, q, k, v, o, lse, w, stream, n=200):
+    """Host microseconds per call, launches not waited for: the raw C-ABI call
+    (ctypes, arguments prepared once) and the Python binding (shape, dtype
+    and device checks, then the same call)."""
+    import ctypes
+
+    import torch
+
+    lib = fa.library()
+    vp = ctypes.c_void_p
+    args = (vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()), vp(lse.data_ptr()),
+            w.B, w.H, w.N, w.d, int(w.causal), float(w.scale), vp(stream.cuda_stream))
+    out = {}
+    for name, call in (("c_abi", lambda: lib.fa_fwd(*args)),
+                       ("binding", lambda: fa.fwd_into(q, k, v, o, lse, w.causal, w.scale))):
+        call()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            call()
+        dt = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        out[name] = round(dt / n * 1e6, 2)
+    return out
+
+
 def cpu_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
     """Times the fp64 oracle on a bounded sample of rows; returns a dict with
     TFLOP/s, the threads used and a description of the sample."""
@@ -312,11 +486,11 @@ def cpu_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
         vis = (rows + 1) if w.causal else np.full_like(rows, w.N)
         return float(np.sum(4.0 * w.d * vis))
 
-    def run(n):
+    def run(n, threads=0):
         bh = rng.integers(0, w.B * w.H, size=n, dtype=np.int64)
         row = rng.integers(0, w.N, size=n, dtype=np.int64)
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, w.causal, w.scale, bh, row)
+        oracle.attention_rows(q, k, v, w.causal, w.scale, bh, row, threads=threads)
         return time.perf_counter() - t0, flops_of(row)
 
     threads = oracle.max_threads()
@@ -329,14 +503,31 @@ def cpu_oracle_rate(w, q, k, v, budget_s: float, seed: int = 7):
     total_n = n
     total_t = dt
     total_f = fl
-    n_big = max(n, int(n * (budget_s - total_t) / max(dt, 1e-9)))
-    if total_t < budget_s:
+    main_budget = 0.8 * budget_s
+    n_big = max(n, int(n * (main_budget - total_t) / max(dt, 1e-9)))
+    if total_t < main_budget:
         dt, fl = run(n_big)
         total_n, total_t, total_f = n_big, dt, fl
         rate = fl / dt
+    # One thread, on a sample sized to the rest of the budget.
+    per_row_one_thread = total_t / total_n * threads  # assumes near-linear thread scaling
+    n1 = max(8, int(0.2 * budget_s / max(per_row_one_thread, 1e-9)))
+    dt1, fl1 = run(n1, threads=1)
+    rate1 = fl1 / dt1
+    full = iomodel_flops(w)
     return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{total_n} random (b,h,row) rows of the same workload, fp64, "
-                      f"{total_t:.1f} s; FLOPs = 4*d*visible keys per row"}
+                      f"{total_t:.1f} s; FLOPs = 4*d*visible keys per row",
+            "single_thread": {"value": rate1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"{n1} random rows, {dt1:.1f} s"},
+            "extrapolated_full_tensor_s": {"all_threads": round(full / rate, 1), "one_thread": round(full / rate1, 1),
+                                           "how": "extrapolated: the workload's FLOPs / the sampled rate"}}
+
+
+def iomodel_flops(w) -> float:
+    from io_aware_attention_gb300 import iomodel
+
+    return iomodel.attention_flops(w.B, w.H, w.N, w.d, w.causal)
 
 
 def decode_bytes(w) -> int:
@@ -619,6 +810,7 @@ def run_bwd(args, w, config, rank, world, local):
     roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
             "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
+            "frac_of_datasheet": round(achieved / DATASHEET_BF16_TFLOPS, 4),
             "kernel": f"fa::bwd::fa_bwd_kernel<{w.d},{str(w.causal).lower()}>; the timed launch is the whole "
                       "fa_bwd call (prepare + main + dQ conversion), so this is a lower bound for the main kernel",
             "traffic": measured_traffic(w.name, "bwd"), "alg_flops_per_launch": flops,
@@ -830,53 +1022,31 @@ def main(argv=None):
         if pg:
             distm.barrier()
 
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks, peak_src = load_peaks()
     q_h, k_h, v_h = make_qkv(w)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(max(args.warmup, 3)):
+    def step():
         fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
     torch.cuda.synchronize()
     if fa.check_device_status() != 0:
         raise RuntimeError("kernel reported a timed-out wait during warm-up")
 
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    barrier()
-    torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop() if sampler else None
-    ms = ev0.elapsed_time(ev1)
+    # ---- the headline: exactly args.steps launches
+    ms, clocks = timed_region(step, args.steps, stream, torch.cuda.current_device() if rank == 0 else None,
+                              barrier, f"fa_fwd {w.name} x{args.steps}")
     if fa.check_device_status() != 0:
         raise RuntimeError("kernel reported a timed-out wait in the timed region")
     ms = max_over_ranks(ms, dev)
     ms_per_step = ms / args.steps
-
-    # Spread of single launches (each bracketed by its own events), after the
-    # timed region: median and standard deviation.
-    singles = []
-    for _ in range(30):
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        fa.fwd_into(q, k, v, o, lse, w.causal, w.scale)
-        b.record(stream)
-        singles.append((a, b))
-    torch.cuda.synchronize()
-    single_ms = [a.elapsed_time(b) for a, b in singles]
-    launch_stats = {"n": len(single_ms), "median_ms": round(statistics.median(single_ms), 5),
-                    "stdev_ms": round(statistics.stdev(single_ms), 5),
-                    "min_ms": round(min(single_ms), 5)}
+    launch_stats = single_launch_stats(step, stream)
     value = job_tflops(flops, world, ms_per_step)
 
     # ---- end to end through the public call with host buffers
@@ -890,7 +1060,9 @@ def main(argv=None):
         n_e2e = max(3, min(args.steps, 20))
         barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("fa_fwd end to end")
         ems = max_over_ranks(pipelined_e2e(n_e2e, host_in, (o, lse), fwd_step), dev)
+        torch.cuda.nvtx.range_pop()
         barrier()
         h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
@@ -898,16 +1070,41 @@ def main(argv=None):
                "ms_per_step": ems, "steps": n_e2e, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "overlap": E2E_OVERLAP}
 
-    peaks, peak_src = load_peaks()
-    achieved = flops / (ms_per_step * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
-    roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
-            "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
-            "kernel": f"fa::fa_fwd_kernel<{w.d},{str(w.causal).lower()}>",
-            "traffic": measured_traffic(w.name),
-            "alg_bytes_per_launch": iomodel.attention_min_bytes(w.B, w.H, w.N, w.d),
-            "alg_flops_per_launch": flops}
+    roof = tensor_roofline(w, flops, ms_per_step, peaks, peak_src, clocks, sms, fwd_kernel_name(w))
+    roof["traffic"] = measured_traffic(w.name)
+    roof["alg_bytes_per_launch"] = iomodel.attention_min_bytes(w.B, w.H, w.N, w.d)
+
+    # ---- beside the headline (default run only): the other half of the
+    # metric (non-causal), the same launch over a seconds-long region (the
+    # power-capped figure), and the other configurations.
+    blocks = {}
+    if not args.no_blocks and args.workload is None and not args.batch:
+        # sustained: the headline launch repeated for args.sustained_seconds
+        n_sus = max(args.steps, int(args.sustained_seconds / (launch_stats["median_ms"] * 1e-3)) + 1)
+        sus_ms, sclocks = timed_region(step, n_sus, stream, torch.cuda.current_device() if rank == 0 else None,
+                                     barrier, f"fa_fwd {w.name} sustained x{n_sus}")
+        if fa.check_device_status() != 0:
+            raise RuntimeError("kernel reported a timed-out wait in the sustained region")
+        sus_per = max_over_ranks(sus_ms, dev) / n_sus
+        sroof = tensor_roofline(w, flops, sus_per, peaks, peak_src, sclocks, sms, fwd_kernel_name(w))
+        if sclocks and sclocks.get("sm_mhz"):
+            # time x clock: launch time at the maximum SM clock, if the work
+            # scaled with the clock
+            sroof["ms_per_step_at_max_clock"] = round(sus_per * sclocks["sm_mhz"] / sclocks["sm_max_mhz"], 5)
+        blocks["sustained"] = {"workload": w.name, "steps": n_sus, "timed_s": round(sus_ms / 1e3, 3),
+                               "ms_per_step": round(sus_per, 5),
+                               "value": round(flops / (sus_per * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                               "roofline": sroof, "clocks": sclocks}
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+        others = [("non_causal", "b8_h32_n4096_d128", {}),
+                  ("config_b1_h2_n256_d64", "b1_h2_n256_d64", {"host_cost": True, "min_steps": 200}),
+                  ("config_b4_h16_n2048_d128_causal", "b4_h16_n2048_d128_causal", {}),
+                  ("config_b1_h32_n32768_d128_causal", "b1_h32_n32768_d128_causal", {}),
+                  ("config_b16_h16_n8192_d64_spiky", "b16_h16_n8192_d64_spiky", {})]
+        for key, name, kw in others:
+            blocks[key] = fwd_block(fa, WORKLOADS[name], dev, stream, peaks, peak_src, sms, rank, barrier, **kw)
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -920,7 +1117,8 @@ def main(argv=None):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": args.steps, "clocks": clocks, "launch_stats": launch_stats,
-                "pct_of_peak": round(100 * achieved / peak, 2)}
+                "pct_of_peak": round(100 * roof["frac"], 2), "datasheet": DATASHEET_SOURCE}
+        line.update(blocks)
         print(json.dumps(line), flush=True)
     if pg:
         distm.destroy_process_group()

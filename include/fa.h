@@ -68,8 +68,11 @@ typedef enum fa_status {
  *   stream   CUDA stream the work is enqueued on.
  *
  * Ownership: the caller allocates and frees every buffer.  The library keeps
- * no per-call state and allocates no device memory; it caches one-time
- * per-device set-up (kernel attributes).
+ * no per-call state and allocates no device memory.  It caches one-time
+ * per-device set-up (kernel attributes, the SM count and L2 size) and, per
+ * host thread, the TMA descriptors of the last few buffers it was given (a
+ * descriptor is a pure function of the address and sizes, so a reused
+ * buffer gets the same descriptor a fresh encode would give).
  *
  * Asynchrony: returns after enqueuing; results are valid once `stream` has
  * been synchronised.  Errors found before the launch are returned directly;
@@ -107,8 +110,11 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
  *   k, v     device pointers, bf16, contiguous (B, H, Nk, d): the cache.
  *   o        device pointer, bf16, contiguous (B, H, Nq, d); fully written.
  *   lse      device pointer, fp32, contiguous (B, H, Nq); fully written.
- *   B, H     batch and heads, B*H <= 65535.  d: 64 or 128.  causal: 0 or 1
- *            (1 requires Nq <= Nk).  scale: finite, > 0.
+ *   B, H     batch and heads, B*H <= 65535.  causal: 0 or 1 (1 requires
+ *            Nq <= Nk).  scale: finite, > 0.
+ *   d        head size: a multiple of 8 from 8 to 128, as for fa_fwd (sizes
+ *            other than 64 and 128 run in the 64- or 128-column kernel with
+ *            the columns past d read as zeros; only d columns are written).
  *   workspace, workspace_bytes
  *            device scratch of at least fa_decode_workspace_bytes(...) bytes,
  *            16-byte aligned (may be NULL when that size is 0).  It holds the
@@ -118,8 +124,10 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
  *
  * Ownership: the caller allocates every buffer, including the workspace; the
  * library allocates nothing.  Asynchrony as for fa_fwd.  Errors: as fa_fwd,
- * plus FA_ERR_INVALID_ARG for a missing or short workspace and
- * FA_ERR_UNSUPPORTED for Nq > 8.
+ * plus FA_ERR_INVALID_ARG for a missing or short workspace, and
+ * FA_ERR_UNSUPPORTED for Nq > 8 or a workspace that is not 16-byte aligned.
+ * The sizes, scale, pointers and overlaps with the inputs are checked before
+ * the device is queried.
  */
 fa_status fa_decode(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                     int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
@@ -139,7 +147,9 @@ fa_status fa_decode(const void *q, const void *k, const void *v, void *o, float 
  *   - Arguments, results and errors are those of fa_decode, minus the
  *     workspace; sizes whose scratch need (fa_decode_workspace_bytes) exceeds
  *     FA_DECODE_STATIC_SCRATCH_BYTES are rejected with FA_ERR_TOO_LARGE and
- *     nothing is enqueued.
+ *     nothing is enqueued.  FA_ERR_TOO_LARGE comes only after every check
+ *     that fa_decode makes before touching the device (sizes, scale,
+ *     pointers, overlaps) has passed.
  *   - The first call on a device looks up the device address of the scratch
  *     array (cudaGetSymbolAddress, with that device current; a failure is
  *     returned as FA_ERR_CUDA), which may load the library's device code.  Make
@@ -198,9 +208,11 @@ fa_status fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t d, siz
  * Bf16 pointers and the workspace 16-byte aligned, lse 4-byte aligned,
  * else FA_ERR_UNSUPPORTED.  Outputs and workspace may overlap no input and
  * no other output (FA_ERR_INVALID_ARG).  Asynchrony, FA_ERR_CUDA and
- * FA_ERR_TIMEOUT reporting as for fa_fwd.  dQ is accumulated in fp32 with
- * element-wise atomic adds, so its last bits may differ between runs; dK and
- * dV are deterministic.
+ * FA_ERR_TIMEOUT reporting as for fa_fwd.  dQ is accumulated in fp32 in the
+ * workspace: each step adds its contribution with one bulk tensor reduce-add
+ * (cp.reduce.async.bulk.tensor, the add done in L2) per block of 64 query
+ * rows and 32 head dims.  The order of those adds depends on timing, so the
+ * last bits of dQ may differ between runs; dK and dV are deterministic.
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                  const void *dout, void *dq, void *dk, void *dv, int64_t B, int64_t H, int64_t N,
@@ -244,6 +256,13 @@ fa_status fa_bias_gelu_dropout(const void *x, const void *bias, const uint32_t *
  * kernel refused to run (shared memory not 1024-byte aligned), FA_OK
  * otherwise.  `where`, if not NULL, receives the code of the first wait that
  * gave up (0 if none).
+ *
+ * The status word is per device, not per stream: it collects the reports of
+ * every kernel of this library on the device, whatever stream launched it,
+ * and the check waits only for `stream`.  Kernels still running on other
+ * streams may report after the read; the clear removes only the bits that
+ * were read (an atomic update on the device), so such a later report stays
+ * for the next check.
  */
 fa_status fa_check_device_status(fa_stream_t stream, uint32_t *where);
 
@@ -275,6 +294,20 @@ fa_status fa_set_wait_limit_ns(uint64_t ns);
  * it off.  Outputs of a launch made with the hook on are incomplete.
  */
 fa_status fa_debug_skip_k_tile(int tile);
+
+/*
+ * fa_debug_set_schedule — test hook for the forward's causal item order.
+ * The persistent forward kernel takes its causal work items either in pairs
+ * (a heavy and a light query block of one head, which keeps that head's K
+ * and V in L2) or in cost order (heaviest first, snaking over the CTAs),
+ * and chooses by size: cost order when all heads' K and V fit in 60% of L2.
+ * order = 0 forces the pair order and 1 the cost order on every later
+ * causal fa_fwd launch (non-causal launches have one order only); -1 (the
+ * default) restores the choice by size.  Both orders compute every row the
+ * same way, so the results are identical to the bit; only the speed
+ * differs.  FA_ERR_INVALID_ARG for any other value.
+ */
+fa_status fa_debug_set_schedule(int order);
 
 /* Static description of a status code (never NULL). */
 const char *fa_status_string(fa_status s);

@@ -18,7 +18,8 @@ recomputing the probabilities from ``lse``.
 
     o, lse = io_aware_attention_gb300.decode(q, k_cache, v_cache, causal=True)
 
-is split-KV decode of up to 8 query rows against a long cache (d 64 or 128).
+is split-KV decode of up to 8 query rows against a long cache (the same head
+sizes).
 
     y = io_aware_attention_gb300.bias_gelu_dropout(x, bias, keep, p)
 
@@ -37,12 +38,12 @@ import os
 from . import _build
 
 __all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "bias_gelu_dropout", "decode", "decode_into", "decode_workspace_bytes", "check_device_status", "get_device_status",
-           "set_wait_limit_ns", "debug_skip_k_tile", "FaError", "library", "library_path", "version", "STATUS"]
+           "set_wait_limit_ns", "debug_skip_k_tile", "debug_set_schedule", "FaError", "library", "library_path", "version", "STATUS"]
 
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
 EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bias_gelu_dropout", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status", "fa_get_device_status",
-           "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_status_string", "fa_version"]
+           "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_debug_set_schedule", "fa_status_string", "fa_version"]
 
 
 class FaError(RuntimeError):
@@ -96,6 +97,8 @@ def library():
     lib.fa_set_wait_limit_ns.restype = ctypes.c_int
     lib.fa_debug_skip_k_tile.argtypes = [ctypes.c_int]
     lib.fa_debug_skip_k_tile.restype = ctypes.c_int
+    lib.fa_debug_set_schedule.argtypes = [ctypes.c_int]
+    lib.fa_debug_set_schedule.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
@@ -356,3 +359,11 @@ def debug_skip_k_tile(tile: int) -> None:
     rc = library().fa_debug_skip_k_tile(int(tile))
     if rc != 0:
         raise FaError(rc, "fa_debug_skip_k_tile")
+
+
+def debug_set_schedule(order: int) -> None:
+    """Test hook: see fa_debug_set_schedule in include/fa.h (-1: the order by
+    size, 0: heavy/light pairs, 1: cost order)."""
+    rc = library().fa_debug_set_schedule(int(order))
+    if rc != 0:
+        raise FaError(rc, "fa_debug_set_schedule")

@@ -23,6 +23,7 @@ constexpr int MAX_DEVICES = 64;
 
 std::atomic<uint64_t> g_wait_limit_ns{DEFAULT_WAIT_LIMIT_NS};
 std::atomic<int> g_debug_skip_k{-1};
+std::atomic<int> g_debug_schedule{-1};  // causal item order: -1 by size, 0 pairs, 1 cost order
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -58,6 +59,42 @@ bool make_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// make_map through a small per-thread cache of recent encodes.  The encode is
+// a pure function of its arguments (address, sizes, box rows; the data type,
+// swizzle and fill are fixed), so a hit returns exactly the map a fresh
+// encode would.  Repeated calls on the same buffers then skip the driver's
+// encode (three per forward call).
+bool cached_map(CUtensorMap* map, const void* base, int64_t BH, int64_t N, int64_t d, uint32_t rows)
+{
+    struct Entry {
+        CUtensorMap map;
+        const void* base;
+        int64_t BH, N, d;
+        uint32_t rows;
+        bool valid;
+    };
+    constexpr int SLOTS = 8;
+    thread_local Entry cache[SLOTS] = {};
+    thread_local unsigned next = 0;
+    for (int i = 0; i < SLOTS; ++i) {
+        const Entry& e = cache[i];
+        if (e.valid && e.base == base && e.BH == BH && e.N == N && e.d == d && e.rows == rows) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!make_map(map, base, BH, N, d, rows)) return false;
+    Entry& e = cache[next++ % SLOTS];
+    e.map = *map;
+    e.base = base;
+    e.BH = BH;
+    e.N = N;
+    e.d = d;
+    e.rows = rows;
+    e.valid = true;
+    return true;
 }
 
 // The backward's fp32 dQ accumulator (B*H, Np, d) as a 3-D tensor; box = 32
@@ -123,27 +160,47 @@ fa_status launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap
     return launch_one<D, CAUSAL, PAD, false>(mq, mk, mv, p, grid, dev, stream);
 }
 
-// Number of SMs of a device (cached): the kernel is persistent, one CTA per SM.
-int sm_count(int dev)
+// Properties of a device that every call needs, queried once per device.
+struct DevInfo {
+    int sms;    // SMs: the persistent kernels run one CTA per SM
+    int l2;     // L2 bytes: picks the causal item order
+    bool sm103; // compute capability 10.3
+};
+
+std::atomic<int> g_devinfo_ready[MAX_DEVICES];
+DevInfo g_devinfo[MAX_DEVICES];
+std::mutex g_devinfo_lock;
+
+// The current device (-1 if it cannot be queried) and its cached properties.
+bool current_device(int* dev_out, DevInfo* info)
 {
-    static std::atomic<int> cache[MAX_DEVICES];
-    if (dev < 0 || dev >= MAX_DEVICES) return 0;
-    int n = cache[dev].load(std::memory_order_relaxed);
-    if (n == 0 && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-        cache[dev].store(n, std::memory_order_relaxed);
-    return n;
+    int dev = -1;
+    *dev_out = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return false;
+    if (!g_devinfo_ready[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> guard(g_devinfo_lock);
+        if (!g_devinfo_ready[dev].load(std::memory_order_relaxed)) {
+            int major = 0, minor = 0, sms = 0, l2 = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || sms <= 0)
+                return false;
+            g_devinfo[dev] = DevInfo{sms, l2, major == 10 && minor == 3};
+            g_devinfo_ready[dev].store(1, std::memory_order_release);
+        }
+    }
+    *dev_out = dev;
+    *info = g_devinfo[dev];
+    return true;
 }
 
-bool device_is_sm103(int* dev_out)
+// FA_OK when the current device is an sm_103 (its properties in *info),
+// FA_ERR_CUDA when it cannot be queried, FA_ERR_UNSUPPORTED otherwise.
+fa_status sm103_device(int* dev, DevInfo* info)
 {
-    int dev = -1, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-        return false;
-    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return false;
-    *dev_out = dev;
-    return major == 10 && minor == 3;
+    if (!current_device(dev, info)) return FA_ERR_CUDA;
+    return info->sm103 ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
 // -------------------------------------------------------------- backward
@@ -222,12 +279,15 @@ struct DecodePlan {
 };
 
 // Splits of the key range: about 8 CTAs per SM over all heads (many short
-// waves, a small tail), each CTA streaming at least 4 rounds of keys.
+// waves, a small tail), each CTA streaming at least 4 rounds of keys.  A
+// round is what the kernel instance for head size Dp (64 or 128) takes in
+// one pass; the workspace holds d columns per partial output.
 DecodePlan decode_plan(int64_t BH, int64_t nq, int64_t nk, int64_t d, int sms)
 {
     DecodePlan pl;
     pl.slots = decode_slots(nq);
-    const int round = fa::dec::WARPS * fa::dec::loads_in_flight(pl.slots) * (32 / (int)(d / 8));
+    const int64_t Dp = padded_head_size(d);
+    const int round = fa::dec::WARPS * fa::dec::loads_in_flight(pl.slots) * (32 / (int)(Dp / 8));
     const int64_t max_splits = std::max<int64_t>(1, (nk + 4 * round - 1) / (4 * round));
     const int64_t want = std::max<int64_t>(1, (8 * (int64_t)sms + BH - 1) / BH);
     int64_t splits = std::min<int64_t>(want, max_splits);
@@ -240,12 +300,13 @@ DecodePlan decode_plan(int64_t BH, int64_t nq, int64_t nk, int64_t d, int sms)
     return pl;
 }
 
+// Checks of the sizes alone (no pointer, no device).
 fa_status decode_check(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal)
 {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!head_size_ok(d)) return FA_ERR_UNSUPPORTED;
     if (Nq > fa::dec::MAX_NQ) return FA_ERR_UNSUPPORTED;
     const int64_t LIM = (int64_t)1 << 62;
     if (B > LIM / H || B * H > LIM / Nk || B * H * Nk > LIM / d) return FA_ERR_INVALID_ARG;
@@ -253,38 +314,15 @@ fa_status decode_check(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, 
     return FA_OK;
 }
 
-template <int D, int QM>
-fa_status launch_decode(const fa::dec::Params& p, int64_t BH, cudaStream_t st)
-{
-    fa::dec::fa_decode_partial_kernel<D, QM>
-        <<<dim3((unsigned)p.splits, (unsigned)BH), fa::dec::THREADS, 0, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    if (p.splits > 1) {
-        fa::dec::fa_decode_combine_kernel<D><<<(unsigned)(BH * p.nq), D, 0, st>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    }
-    return FA_OK;
-}
-
-template <int D>
-fa_status launch_decode_d(const fa::dec::Params& p, int slots, int64_t BH, cudaStream_t st)
-{
-    switch (slots) {
-    case 1: return launch_decode<D, 1>(p, BH, st);
-    case 2: return launch_decode<D, 2>(p, BH, st);
-    case 4: return launch_decode<D, 4>(p, BH, st);
-    default: return launch_decode<D, 8>(p, BH, st);
-    }
-}
-
-// Decode with an explicit workspace (ws, ws_bytes >= the plan's).
-fa_status decode_run(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
-                     int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, void* ws,
-                     size_t ws_bytes, fa_stream_t stream)
+// Every check that needs no device: sizes, scale, null and misaligned
+// pointers, outputs overlapping inputs.  The workspace is checked against
+// the plan later (its size depends on the device).
+fa_status decode_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int64_t B,
+                      int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, const void* ws)
 {
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    fa_status st_chk = decode_check(B, H, Nq, Nk, d, causal);
-    if (st_chk != FA_OK) return st_chk;
+    const fa_status st = decode_check(B, H, Nq, Nk, d, causal);
+    if (st != FA_OK) return st;
     if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
@@ -295,12 +333,46 @@ fa_status decode_run(const void* q, const void* k, const void* v, void* o, float
     if (overlaps(o, qb, q, qb) || overlaps(o, qb, k, kb) || overlaps(o, qb, v, kb) || overlaps(o, qb, lse, lb) ||
         overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb))
         return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
 
+template <int D, int QM, bool PAD>
+fa_status launch_decode(const fa::dec::Params& p, int64_t BH, cudaStream_t st)
+{
+    fa::dec::fa_decode_partial_kernel<D, QM, PAD>
+        <<<dim3((unsigned)p.splits, (unsigned)BH), fa::dec::THREADS, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    if (p.splits > 1) {
+        fa::dec::fa_decode_combine_kernel<D><<<(unsigned)(BH * p.nq), D, 0, st>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return FA_OK;
+}
+
+template <int D, bool PAD>
+fa_status launch_decode_d(const fa::dec::Params& p, int slots, int64_t BH, cudaStream_t st)
+{
+    switch (slots) {
+    case 1: return launch_decode<D, 1, PAD>(p, BH, st);
+    case 2: return launch_decode<D, 2, PAD>(p, BH, st);
+    case 4: return launch_decode<D, 4, PAD>(p, BH, st);
+    default: return launch_decode<D, 8, PAD>(p, BH, st);
+    }
+}
+
+// Decode with an explicit workspace (ws, ws_bytes >= the plan's), once the
+// arguments have passed decode_args.
+fa_status decode_run(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                     int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, void* ws,
+                     size_t ws_bytes, fa_stream_t stream)
+{
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
-    const DecodePlan pl = decode_plan(BH, Nq, Nk, d, sms);
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
+    const int64_t BH = B * H;
+    const size_t qb = (size_t)(BH * Nq * d * 2), kb = (size_t)(BH * Nk * d * 2), lb = (size_t)(BH * Nq * 4);
+    const DecodePlan pl = decode_plan(BH, Nq, Nk, d, info.sms);
     if (pl.ws_bytes > 0) {
         if (!ws || ws_bytes < pl.ws_bytes) return FA_ERR_INVALID_ARG;
         if (overlaps(ws, pl.ws_bytes, o, qb) || overlaps(ws, pl.ws_bytes, lse, lb) || overlaps(ws, pl.ws_bytes, q, qb) ||
@@ -318,12 +390,17 @@ fa_status decode_run(const void* q, const void* k, const void* v, void* o, float
     p.ws_lse = pl.ws_bytes > 0 ? static_cast<float*>(ws) + (size_t)(BH * Nq * pl.splits) * (size_t)d : nullptr;
     p.nq = (int)Nq;
     p.nk = (int)Nk;
+    p.d = (int)d;
     p.splits = pl.splits;
     p.chunk = pl.chunk;
     p.causal = causal;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return d == 128 ? launch_decode_d<128>(p, pl.slots, BH, st) : launch_decode_d<64>(p, pl.slots, BH, st);
+    // Head sizes below 64 or 128 run in that instance with the columns past d
+    // read as zeros (PAD).
+    if (d == 128) return launch_decode_d<128, false>(p, pl.slots, BH, st);
+    if (d == 64) return launch_decode_d<64, false>(p, pl.slots, BH, st);
+    return d > 64 ? launch_decode_d<128, true>(p, pl.slots, BH, st) : launch_decode_d<64, true>(p, pl.slots, BH, st);
 }
 
 // Scratch of fa_decode_static: compiled into the library, one per device.
@@ -347,6 +424,14 @@ void* static_scratch(int dev)
     return p;
 }
 
+// Clears the status bits a check has read (and the wait code, if it is still
+// the one read), leaving bits that kernels on other streams set since.
+__global__ void fa_clear_status_kernel(unsigned int bits, unsigned int where)
+{
+    atomicAnd(&fa::g_status, ~bits);
+    atomicCAS(&fa::g_status_where, where, 0u);
+}
+
 }  // namespace
 
 extern "C" {
@@ -355,14 +440,15 @@ fa_status fa_decode_static(const void* q, const void* k, const void* v, void* o,
                            int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, float scale,
                            fa_stream_t stream)
 {
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    fa_status st = decode_check(B, H, Nq, Nk, d, causal);
+    // The argument checks come first, so that a call fa_decode would refuse
+    // gets the same status here, whatever its sizes.
+    const fa_status st = decode_args(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, nullptr);
     if (st != FA_OK) return st;
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
-    const size_t need = decode_plan(B * H, Nq, Nk, d, sms).ws_bytes;
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
+    const size_t need = decode_plan(B * H, Nq, Nk, d, info.sms).ws_bytes;
     if (need > FA_DECODE_STATIC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
     void* scratch = static_scratch(dev);
     if (!scratch) return FA_ERR_CUDA;
@@ -374,13 +460,13 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
                                     size_t* bytes)
 {
     if (!bytes) return FA_ERR_INVALID_ARG;
-    fa_status st = decode_check(B, H, Nq, Nk, d, causal);
+    const fa_status st = decode_check(B, H, Nq, Nk, d, causal);
     if (st != FA_OK) return st;
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
-    *bytes = decode_plan(B * H, Nq, Nk, d, sms).ws_bytes;
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
+    *bytes = decode_plan(B * H, Nq, Nk, d, info.sms).ws_bytes;
     return FA_OK;
 }
 
@@ -388,9 +474,10 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     int64_t Nq, int64_t Nk, int64_t d, int causal, float scale, void* workspace,
                     size_t workspace_bytes, fa_stream_t stream)
 {
+    const fa_status st = decode_args(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, workspace);
+    if (st != FA_OK) return st;
     return decode_run(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, workspace, workspace_bytes, stream);
 }
-
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                  int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream)
@@ -418,14 +505,14 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
     // ---- device
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
 
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, q, BH, N, d, fa::BM) || !make_map(&mk, k, BH, N, d, fa::BN) ||
-        !make_map(&mv, v, BH, N, d, fa::BN))
+    if (!cached_map(&mq, q, BH, N, d, fa::BM) || !cached_map(&mk, k, BH, N, d, fa::BN) ||
+        !cached_map(&mv, v, BH, N, d, fa::BN))
         return FA_ERR_CUDA;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
 
     fa::Params p;
     p.o = static_cast<__nv_bfloat16*>(o);
@@ -441,12 +528,12 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     // Causal items differ in cost.  Heavy/light pairs of a head keep its K/V
     // in L2 while its blocks run; when all heads' K and V fit in L2 anyway,
     // ordering the items by cost balances the CTAs better (see item_of).
-    int l2_bytes = 0;
-    if (cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return FA_ERR_CUDA;
+    // (fa_debug_set_schedule may force either order for tests.)
     const double kv_bytes = 2.0 * (double)BH * (double)N * (double)d * 2.0;
-    const bool snake = causal && kv_bytes <= 0.6 * (double)l2_bytes;
+    const int forced = g_debug_schedule.load(std::memory_order_relaxed);
+    const bool snake = causal && (forced < 0 ? kv_bytes <= 0.6 * (double)info.l2 : forced == 1);
     // One CTA per SM, at most one per work item (per pair of items in pair order).
-    const unsigned grid = (unsigned)std::min<int64_t>(snake ? BH * m_blocks : (BH * m_blocks + 1) / 2, sms);
+    const unsigned grid = (unsigned)std::min<int64_t>(snake ? BH * m_blocks : (BH * m_blocks + 1) / 2, info.sms);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
     if (d == 128)
@@ -506,15 +593,16 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
     // ---- device
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
+    const int sms = info.sms;
     float* const lse2 = static_cast<float*>(workspace);
     float* const dsum = lse2 + BH * sh.Np;
     float* const acc = dsum + BH * sh.Np;
     CUtensorMap mq, mk, mv, mdo, mdq;
-    if (!make_map(&mq, q, BH, N, d, fa::bwd::BQ) || !make_map(&mk, k, BH, N, d, fa::bwd::BKV) ||
-        !make_map(&mv, v, BH, N, d, fa::bwd::BKV) || !make_map(&mdo, dout, BH, N, d, fa::bwd::BQ) ||
+    if (!cached_map(&mq, q, BH, N, d, fa::bwd::BQ) || !cached_map(&mk, k, BH, N, d, fa::bwd::BKV) ||
+        !cached_map(&mv, v, BH, N, d, fa::bwd::BKV) || !cached_map(&mdo, dout, BH, N, d, fa::bwd::BQ) ||
         !make_acc_map(&mdq, acc, BH, sh.Np, sh.Dp))
         return FA_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -576,9 +664,10 @@ fa_status fa_bias_gelu_dropout(const void* x, const void* bias, const uint32_t* 
         return FA_ERR_INVALID_ARG;
 
     int dev = -1;
-    if (!device_is_sm103(&dev)) return dev < 0 ? FA_ERR_CUDA : FA_ERR_UNSUPPORTED;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FA_ERR_CUDA;
+    DevInfo info;
+    const fa_status ds = sm103_device(&dev, &info);
+    if (ds != FA_OK) return ds;
+    const int sms = info.sms;
 
     fa::ew::Params prm;
     prm.x = static_cast<const __nv_bfloat16*>(x);
@@ -614,7 +703,6 @@ fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
 {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     unsigned int h[2] = {0u, 0u};
-    const unsigned int zero[2] = {0u, 0u};
     if (cudaMemcpyFromSymbolAsync(&h[0], fa::g_status, sizeof(unsigned int), 0,
                                   cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaMemcpyFromSymbolAsync(&h[1], fa::g_status_where, sizeof(unsigned int), 0,
@@ -624,16 +712,16 @@ fa_status fa_check_device_status(fa_stream_t stream, uint32_t* where)
     if (where) *where = h[1];
     if (h[0] != 0u) {
         const fa_status st_code = (h[0] & fa::STATUS_TIMEOUT) ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
-        if (cudaMemcpyToSymbolAsync(fa::g_status, &zero[0], sizeof(unsigned int), 0,
-                                    cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaMemcpyToSymbolAsync(fa::g_status_where, &zero[1], sizeof(unsigned int), 0,
-                                    cudaMemcpyHostToDevice, st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-            return FA_ERR_CUDA;
+        // Clear what was read, atomically on the device: a bit that a kernel
+        // on another stream set in between stays for the next check.
+        fa_clear_status_kernel<<<1, 1, 0, st>>>(h[0], h[1]);
+        if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
         return st_code;
     }
     return FA_OK;
 }
+
+fa_status fa_get_device_status(fa_stream_t stream) { return fa_check_device_status(stream, nullptr); }
 
 fa_status fa_set_wait_limit_ns(uint64_t ns)
 {
@@ -645,6 +733,13 @@ fa_status fa_debug_skip_k_tile(int tile)
 {
     if (tile < -1) return FA_ERR_INVALID_ARG;
     g_debug_skip_k.store(tile, std::memory_order_relaxed);
+    return FA_OK;
+}
+
+fa_status fa_debug_set_schedule(int order)
+{
+    if (order < -1 || order > 1) return FA_ERR_INVALID_ARG;
+    g_debug_schedule.store(order, std::memory_order_relaxed);
     return FA_OK;
 }
 

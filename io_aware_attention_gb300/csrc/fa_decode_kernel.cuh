@@ -21,6 +21,11 @@
 // rounded).  Loads: a group of G = d/8 lanes owns one key row (16 bytes per
 // lane, one coalesced row per group), and every lane keeps U rows of K and of
 // V in flight.
+//
+// Head sizes d below D (multiples of 8) run in the D = 64 or 128 instance
+// with PAD: rows are d elements apart, the lanes whose 8 columns lie past d
+// load nothing and hold zeros (which add nothing to any dot product), and
+// only d columns are written.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -48,14 +53,15 @@ struct Cfg {
 };
 
 struct Params {
-    const __nv_bfloat16* q;  // (B*H, Nq, D)
-    const __nv_bfloat16* k;  // (B*H, Nk, D)
+    const __nv_bfloat16* q;  // (B*H, Nq, d)
+    const __nv_bfloat16* k;  // (B*H, Nk, d)
     const __nv_bfloat16* v;
-    __nv_bfloat16* o;        // (B*H, Nq, D), written when splits == 1
+    __nv_bfloat16* o;        // (B*H, Nq, d), written when splits == 1
     float* lse;              // (B*H, Nq), written when splits == 1
-    float* ws_o;             // (B*H*Nq, splits, D) partial outputs (normalised)
+    float* ws_o;             // (B*H*Nq, splits, d) partial outputs (normalised)
     float* ws_lse;           // (B*H*Nq, splits) partial logsumexps (natural log)
     int nq, nk, splits, chunk;  // chunk: keys per split (a multiple of ROUND)
+    int d;                   // the caller's head size (<= D): row stride and columns present
     int causal;
     float scale_log2;        // scale * log2(e)
 };
@@ -89,7 +95,7 @@ __device__ __forceinline__ float ex2f(float x)
 }
 
 // Partial attention of one (head, chunk) for QM query slots (Nq <= QM).
-template <int D, int QM>
+template <int D, int QM, bool PAD>
 __global__ void __launch_bounds__(THREADS)
     fa_decode_partial_kernel(const Params p)
 {
@@ -100,13 +106,15 @@ __global__ void __launch_bounds__(THREADS)
     const int nq = p.nq, nk = p.nk;
     const int k_begin = split * p.chunk;
     const int k_end = min(nk, k_begin + p.chunk);
+    const int dd = PAD ? p.d : D;              // row stride and columns present
+    const bool cols_ok = !PAD || sub * 8 < dd;  // this lane's columns exist
 
     // This lane's 8 columns of each query row, times scale * log2(e).
     float qv[QM][8];
 #pragma unroll
     for (int i = 0; i < QM; ++i) {
-        if (i < nq) {
-            const uint4 w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)bh * nq + i) * D + sub * 8);
+        if (i < nq && cols_ok) {
+            const uint4 w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)bh * nq + i) * dd + sub * 8);
             unpack8(w, qv[i]);
 #pragma unroll
             for (int e = 0; e < 8; ++e) qv[i][e] *= p.scale_log2;
@@ -125,8 +133,8 @@ __global__ void __launch_bounds__(THREADS)
         for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
     }
 
-    const __nv_bfloat16* const kh = p.k + (int64_t)bh * nk * D + sub * 8;
-    const __nv_bfloat16* const vh = p.v + (int64_t)bh * nk * D + sub * 8;
+    const __nv_bfloat16* const kh = p.k + (int64_t)bh * nk * dd + sub * 8;
+    const __nv_bfloat16* const vh = p.v + (int64_t)bh * nk * dd + sub * 8;
     for (int r0 = k_begin; r0 < k_end; r0 += C::ROUND) {
         // Key of load u: rows of one warp are consecutive (KPW per load).
         uint4 kw[C::U], vw[C::U];
@@ -135,12 +143,12 @@ __global__ void __launch_bounds__(THREADS)
         for (int u = 0; u < C::U; ++u) {
             key[u] = r0 + (warp * C::U + u) * C::KPW + grp;
             const int kc = min(key[u], k_end - 1);  // rows past the chunk: a valid row, masked below
-            kw[u] = ldg_stream(kh + (int64_t)kc * D);
+            kw[u] = cols_ok ? ldg_stream(kh + (int64_t)kc * dd) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < C::U; ++u) {
             const int kc = min(key[u], k_end - 1);
-            vw[u] = ldg_stream(vh + (int64_t)kc * D);
+            vw[u] = cols_ok ? ldg_stream(vh + (int64_t)kc * dd) : make_uint4(0u, 0u, 0u, 0u);
         }
         // Scores s[i][u] (base 2), reduced over the G lanes of the group.
         float s[QM][C::U];
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(THREADS)
     __syncthreads();
     for (int t = threadIdx.x; t < QM * D; t += THREADS) {
         const int i = t / D, c = t % D;
-        if (i >= nq) continue;
+        if (i >= nq || c >= dd) continue;
         float mx = -INFINITY;
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, sm_m[w][i]);
@@ -241,21 +249,24 @@ __global__ void __launch_bounds__(THREADS)
         const float lse_s = (lt > 0.f) ? (mx + __log2f(lt)) * LN2 : -INFINITY;
         const float o_s = (lt > 0.f) ? ot / lt : 0.f;
         if (p.splits == 1) {
-            p.o[row * D + c] = __float2bfloat16_rn(o_s);
+            p.o[row * dd + c] = __float2bfloat16_rn(o_s);
             if (c == 0) p.lse[row] = lse_s;
         } else {
-            p.ws_o[(row * p.splits + split) * D + c] = o_s;
+            p.ws_o[(row * p.splits + split) * dd + c] = o_s;
             if (c == 0) p.ws_lse[row * p.splits + split] = lse_s;
         }
     }
 }
 
-// Merge of the splits of one query row: block of D threads, one column each.
+// Merge of the splits of one query row: block of D threads, one column each
+// (the columns past the head size d idle).
 template <int D>
 __global__ void __launch_bounds__(D) fa_decode_combine_kernel(const Params p)
 {
     const int64_t row = blockIdx.x;  // (bh, query)
     const int c = threadIdx.x;
+    const int dd = p.d;
+    if (c >= dd) return;
     const float* const ls = p.ws_lse + row * p.splits;
     float mx = -INFINITY;
     for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, ls[s]);
@@ -263,9 +274,9 @@ __global__ void __launch_bounds__(D) fa_decode_combine_kernel(const Params p)
     for (int s = 0; s < p.splits; ++s) {
         const float w = (ls[s] == -INFINITY) ? 0.f : __expf(ls[s] - mx);
         wsum += w;
-        ot += w * p.ws_o[(row * p.splits + s) * D + c];
+        ot += w * p.ws_o[(row * p.splits + s) * dd + c];
     }
-    p.o[row * D + c] = __float2bfloat16_rn(ot / wsum);
+    p.o[row * dd + c] = __float2bfloat16_rn(ot / wsum);
     if (c == 0) p.lse[row] = mx + __logf(wsum);
 }
 

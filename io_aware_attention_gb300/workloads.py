@@ -58,6 +58,13 @@ WORKLOADS = {
         Workload("b1_h32_n32768_d128_causal", 1, 32, 32768, 128, True, 1004, sample_rows=256),
         Workload("b16_h16_n8192_d64_spiky", 16, 16, 8192, 64, False, 1005, q_mult=4.0,
                  spike_every=512, spike_mult=8.0, sample_rows=512),
+        # Sequence lengths that are not a multiple of the 128-row tile ("Writing
+        # and Benchmarking Custom Kernels" §10.3.1: the final partial tile):
+        # 4000 = 31 tiles + 32 rows, 4097 = 32 tiles + 1 row.
+        Workload("b8_h32_n4000_d128_causal", 8, 32, 4000, 128, True, 1007, sample_rows=512),
+        Workload("b8_h32_n4000_d128", 8, 32, 4000, 128, False, 1008, sample_rows=512),
+        Workload("b8_h32_n4097_d128_causal", 8, 32, 4097, 128, True, 1009, sample_rows=512),
+        Workload("b8_h32_n4097_d128", 8, 32, 4097, 128, False, 1010, sample_rows=512),
     )
 }
 

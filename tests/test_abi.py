@@ -112,6 +112,13 @@ def test_debug_hook_setter(lib):
     assert lib.fa_debug_skip_k_tile(-1) == 0
 
 
+def test_schedule_hook_setter(lib):
+    assert lib.fa_debug_set_schedule(-2) == 1
+    assert lib.fa_debug_set_schedule(2) == 1
+    for order in (0, 1, -1):
+        assert lib.fa_debug_set_schedule(order) == 0
+
+
 def call_decode(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, Nq=1, Nk=64, d=128, causal=0,
                 scale=0.125, ws=6 * P, ws_bytes=1 << 20):
     vp = ctypes.c_void_p
@@ -123,7 +130,7 @@ def call_decode(lib, q=P, k=2 * P, v=3 * P, o=4 * P, lse=5 * P, B=1, H=1, Nq=1, 
     (dict(q=0), 1), (dict(k=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
     (dict(B=0), 1), (dict(Nq=0), 1), (dict(Nk=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
     (dict(causal=1, Nq=4, Nk=3), 1),   # the causal window needs Nq <= Nk
-    (dict(d=96), 2), (dict(Nq=9), 2),  # head size, more than 8 query rows
+    (dict(d=100), 2), (dict(d=136), 2), (dict(Nq=9), 2),  # head size, more than 8 query rows
     (dict(q=P + 8), 2), (dict(lse=5 * P + 2), 2), (dict(ws=6 * P + 4), 2),
     (dict(o=3 * P + 16), 1),           # o overlaps v
     (dict(B=70000), 1),                # B*H over the grid's 65535
@@ -139,6 +146,25 @@ def test_static_decode_checks_arguments_first(lib):
                                 None) == 1
     assert lib.fa_decode_static(vp(P), vp(2 * P), vp(3 * P), vp(4 * P), vp(5 * P), 1, 1, 9, 64, 128, 0, 0.1,
                                 None) == 2
+
+
+def test_static_decode_argument_errors_come_before_the_size_check(lib):
+    """fa_decode_static gives a call that fa_decode would refuse the same
+    status, at sizes whose scratch need exceeds the static array (B*H = 1215
+    heads of 8 query rows: two splits each, about 10 MB of partial results):
+    the scale, alignment and overlap checks run before the device is queried
+    and before FA_ERR_TOO_LARGE is considered."""
+    vp = ctypes.c_void_p
+
+    def call(q=P, o=4 * P, lse=5 * P, scale=0.1):
+        return lib.fa_decode_static(vp(q), vp(2 * P), vp(3 * P), vp(o), vp(lse), 1215, 1, 8, 4096, 128, 0, scale,
+                                    None)
+
+    assert call(scale=float("nan")) == 1
+    assert call(scale=-1.0) == 1
+    assert call(q=P + 8) == 2
+    assert call(lse=5 * P + 2) == 2
+    assert call(o=3 * P + 16) == 1  # o overlaps v
 
 
 def test_decode_workspace_query_checks_arguments(lib):

@@ -68,6 +68,37 @@ def test_decode_matches_oracle(d, nq, nk, causal):
     assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"d{d} nq{nq} nk{nk} c{int(causal)}")
 
 
+@pytest.mark.parametrize("d", [8, 40, 80, 96, 112])
+@pytest.mark.parametrize("nq", [1, 5])
+@pytest.mark.parametrize("nk", [129, 4097])
+@pytest.mark.parametrize("causal", [False, True])
+def test_decode_padded_head_sizes(d, nq, nk, causal):
+    """Head sizes other than 64 and 128 (multiples of 8) run in the 64- or
+    128-column kernel with the columns past d read as zeros; canary bands
+    around the outputs show any write past d columns or with the padded
+    row stride."""
+    q, k, v = rand(2, 3, nq, nk, d, seed=7000 + nq * 100 + nk + d + int(causal))
+    scale = 1.0 / np.sqrt(d)
+    o, lse, _ = run_guarded(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    o_ref, lse_ref = oracle.attention_rect(q, k, v, causal, scale)
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"d{d} nq{nq} nk{nk} c{int(causal)}")
+
+
+def test_decode_padding_is_exact():
+    """d = 96 equals d = 128 with the last 32 columns of q, k, v zero (the
+    scale kept), bit for bit, both with one split and with many; the padded
+    columns of the d = 128 output are zero."""
+    pad = lambda t: torch.nn.functional.pad(t, (0, 128 - 96)).contiguous()
+    for B, H, nk in ((64, 16, 3000), (1, 1, 20000)):
+        q, k, v = (t.cuda() for t in rand(B, H, 3, nk, 96, seed=B + nk))
+        o96, l96 = fa.decode(q, k, v, causal=True, scale=96 ** -0.5)
+        o128, l128 = fa.decode(pad(q), pad(k), pad(v), causal=True, scale=96 ** -0.5)
+        torch.cuda.synchronize()
+        assert torch.equal(o96, o128[..., :96].contiguous())
+        assert torch.equal(l96, l128)
+        assert (o128[..., 96:] == 0).all()
+
+
 def test_split_and_unsplit_key_ranges():
     """Many heads (one split each) and one head (many splits) give the oracle."""
     for B, H in ((64, 16), (1, 1)):
