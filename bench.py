@@ -77,18 +77,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "212234e8798c71e3aac80fdb0023d789c586c6b7ac95772f427318bbcda6042c",
-        "bytes": 4 * (201_396_480 + 43_813_632),
+        "sha256": "739d954fa9f1cd23469ea7127bc3851d2e7a062bb4a0f34237b2bf322031a83a",
+        "bytes": 4 * (201_448_192 + 45_600_000),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "beb98f5fad0584d3139a0dca8bc5c3c2960a589a8603c7e8557f75aababeb890",
-        "bytes": 4 * (406_242_304 + 217_843_200),
+        "sha256": "45b03688b85a63656652404595c81e41128253f757bc8a0213092bd1ea3858f0",
+        "bytes": 4 * (406_192_128 + 217_494_272),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "4555719982ca73e5e9858fa100bf10c3818f7169290012aa2bcc0d36d2bdc9bd",
-        "bytes": 285_265_408 + 210_365_952,
+        "sha256": "f7df67582338d11f98f8d715252075973271aa1bf134ae2a4433edfc6805e5d6",
+        "bytes": 285_242_368 + 210_490_368,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

@@ -1,17 +1,17 @@
 """Happens-before model of the attention-forward kernel's pipeline (CPU only).
 
 fa_fwd_kernel.cuh coordinates a TMA producer warp, a score-MMA issuer, a
-P.V-MMA issuer and eight softmax warps through mbarriers (waited on by
-parity), hardware named barriers and the asynchronous completion of TMA
-copies and tcgen05 MMAs.  This test replays every role's sequence of barrier
+P.V-MMA issuer, eight softmax warps and four epilogue warps through
+mbarriers (waited on by parity), hardware named barriers and the
+asynchronous completion of TMA copies and tcgen05 MMAs.  This test replays every role's sequence of barrier
 operations and buffer accesses in the order the kernel executes them, under
 random interleavings and random completion times of the copies and MMAs, and
 checks:
 
 * no data race: every two conflicting accesses to a buffer (the Q, K and V
   stages in shared memory; the S, P and O regions of TMEM per lane quarter
-  and half row; the row-max, row-sum and epilogue exchange slots) are ordered
-  by happens-before.  Vector clocks travel through mbarrier phases, named
+  and half row; the row-max exchange slots and the two statistics slots the
+  softmax warps hand to the epilogue warps) are ordered by happens-before.  Vector clocks travel through mbarrier phases, named
   barrier generations, MMA commits and TMA completions (the model and its
   rules are in _pipeline_model.py);
 * parity safety: a wait for phase n of an mbarrier (parity n mod 2) starts
@@ -23,7 +23,9 @@ checks:
 
 Both designs are modelled: d = 128 (one softmax state per row split over two
 warps, a P buffer, S released once read) and the d = 64 split design (two
-independent half-row states, P over S, S released once P.V is done).  Planted
+independent half-row states, P over S, S released once P.V is done); in
+both, the softmax warps leave each item's statistics in one of two slots
+and the epilogue warps read them, then O once the item's last P.V is done.  Planted
 protocol mistakes -- each a single wait or barrier left out -- are caught,
 which shows that the check can fail.  Only the healthy path is modelled; the
 abort path of the named barriers is checked in test_barrier_protocol.py.
@@ -39,9 +41,15 @@ VSTAGES = {128: 2, 64: 4}
 WARPS = 8  # softmax warps: warp w serves lane quarter w % 4, half row w // 4
 
 
+EPI_WARPS = 4  # epilogue warps: warp 8 + q serves lane quarter q
+
+
 def mbarrier_counts(split):
     """Expected arrivals per phase, as the kernel initialises them."""
-    c = {"QFULL": 1, "QEMPTY": 1, "OFINAL": 1, "OFREE": WARPS, "DRAIN0": 1, "DRAIN1": 1}
+    c = {"QFULL": 1, "QEMPTY": 1, "OFINAL": 1, "OFREE": EPI_WARPS, "DRAIN0": 1, "DRAIN1": 1}
+    for slot in range(2):
+        c[f"STFULL{slot}"] = WARPS
+        c[f"STFREE{slot}"] = EPI_WARPS
     for s in range(max(KSTAGES.values())):
         c[f"KFULL{s}"] = c[f"KEMPTY{s}"] = 1
     for s in range(max(VSTAGES.values())):
@@ -74,9 +82,14 @@ def producer(items, D, mut):
         yield ("tma", f"VFULL{s}", gv // VS, [f"V{s}"])
         gv += 1
 
-    for k, n in enumerate(items):
-        yield ("wait", "QEMPTY", k - 1)
+    def load_q(k):
+        # Q of item k once every score MMA of item k - 1 is done
+        yield ("wait", "QEMPTY", k - (2 if mut == "q_early" else 1))
         yield ("tma", "QFULL", k, ["Q"])
+
+    if items:
+        yield from load_q(0)
+    for k, n in enumerate(items):
         for _ in range(n):
             s = gk % KS
             yield ("wait", f"KEMPTY{s}", gk // KS - (2 if mut == "k_early" else 1))
@@ -84,6 +97,9 @@ def producer(items, D, mut):
             gk += 1
             if gv <= gk - 3:
                 yield from issue_v()
+        # the next item's Q ahead of this item's last V loads
+        if k + 1 < len(items):
+            yield from load_q(k + 1)
         while gv < gk:
             yield from issue_v()
     # drain: every copy lands before the CTA exits
@@ -197,24 +213,35 @@ def softmax_warp(w, items, D, split, need, mut):
                 yield ("wr", f"P.{q}.{h}")
                 yield ("arrive", "PFULL", g)
             g += 1
-        # epilogue
+        # the item's statistics to the epilogue warps: slot k & 1, once the
+        # epilogue warps have read what it held two items ago
+        one = mut == "one_slot_no_free"
+        slot = 0 if one else k & 1
+        if mut != "no_stfree" and not one:
+            yield ("wait", f"STFREE{slot}", (k >> 1) - 1)
+        yield ("wr", f"ST{slot}.{q}.{h}")
+        yield ("arrive", f"STFULL{slot}", k if one else k >> 1)
+
+
+def epilogue_warp(q, items, split, mut):
+    """Warp 8 + q: the statistics of lane quarter q, then (once the item's
+    last P.V is done) O and l~ of its rows; O_FREE once they are read."""
+    for k, n in enumerate(items):
+        one = mut == "one_slot_no_free"
+        slot = 0 if one else k & 1
+        phase = k if one else k >> 1
+        yield ("wait", f"STFULL{slot}", phase)
+        yield ("rd", f"ST{slot}.{q}.0")
+        yield ("rd", f"ST{slot}.{q}.1")
+        yield ("arrive", f"STFREE{slot}", phase)
         if mut != "no_ofinal":
             yield ("wait", "OFINAL", k)
         if split:
-            slot = 0 if mut == "one_xch_slot" else k & 1
-            yield ("rd", f"L{h}.{q}")
-            yield ("wr", f"X{slot}.{q}.{h}")
-            if mut != "no_pair":
-                yield ("nb_sync", 1 + q, 2)
-            yield ("rd", f"X{slot}.{q}.{h ^ 1}")
-            yield ("rd", f"O0.{q}.{h}")
-            yield ("rd", f"O1.{q}.{h}")
+            for r in (f"O0.{q}.0", f"O0.{q}.1", f"L0.{q}", f"O1.{q}.0", f"O1.{q}.1", f"L1.{q}"):
+                yield ("rd", r)
         else:
-            yield ("wr", f"LX.{q}.{h}")
-            yield ("nb_sync", 1 + q, 2)
-            yield ("rd", f"LX.{q}.0")
-            yield ("rd", f"LX.{q}.1")
-            yield ("rd", f"O.{q}.{h}")
+            yield ("rd", f"O.{q}.0")
+            yield ("rd", f"O.{q}.1")
         yield ("arrive", "OFREE", k)
 
 
@@ -234,6 +261,8 @@ def simulate(D, seed, items=None, mut=None):
     }
     for w in range(WARPS):
         roles[f"softmax{w}"] = softmax_warp(w, items, D, split, need, mut)
+    for q in range(EPI_WARPS):
+        roles[f"epilogue{q}"] = epilogue_warp(q, items, split, mut)
     Model(mbarrier_counts(split), seed).run(roles)
 
 
@@ -257,12 +286,14 @@ MUTANTS = [
     ((128, 64), "no_s_release", "the score issuer reuses an S buffer without waiting for its readers"),
     ((128,), "no_odone", "P is written before the previous P.V has read the P buffer"),
     ((128, 64), "no_rescale_wait", "O is rescaled while the previous P.V may still add to it"),
-    ((128, 64), "no_pair", "the partner's row max (d = 128) or epilogue values (split) are read "
-                           "without the pair barrier"),
+    ((128,), "no_pair", "the partner's row max is read without the pair barrier"),
     ((64,), "pv_one_half", "a half's P.V waits for the other half's P only"),
-    ((64,), "no_ofree", "the next item's first P.V overwrites O before the other half's epilogue read it"),
-    ((128, 64), "no_ofinal", "the epilogue reads O before the item's last P.V is done"),
+    ((128, 64), "no_ofree", "the next item's first P.V overwrites O before the epilogue warps read it"),
+    ((128, 64), "no_ofinal", "the epilogue warps read O before the item's last P.V is done"),
     ((128, 64), "k_early", "the producer refills a K stage one phase too early"),
+    ((128, 64), "q_early", "the producer loads the next item's Q before the last score MMA read Q"),
+    ((64,), "no_stfree", "the softmax warps overwrite a statistics slot before the epilogue read it"),
+    ((128, 64), "one_slot_no_free", "one statistics slot, reused without waiting until it has been read"),
 ]
 
 
@@ -280,16 +311,12 @@ def test_planted_protocol_mistakes_are_caught(designs, mut, what):
 
 
 def test_redundant_orderings():
-    """Two orderings the kernel spells out are implied by others:
-    - at d = 128 the P.V issuer's wait for "O read out": the first P.V of the
-      next item waits for P-full, and each of the eight softmax warps arrives
-      on it only after its own epilogue has read O (in the split design it is
-      needed: a half's P.V waits for that half's four warps only, while the
-      other half's epilogue reads both accumulators);
-    - in the split design, one epilogue exchange slot instead of one per item
-      parity: the partner reads the slot before it arrives on "O read out",
-      and the next write follows "O final" of the next item, which the P.V
-      issuer commits only after waiting for "O read out"."""
+    """At d = 128 the softmax warps' wait for a free statistics slot is
+    implied by other waits: the statistics of item k + 2 are written after P
+    of item k + 2, whose write waited for a P.V of item k + 1 or later; those
+    P.Vs follow the first P.V of item k + 1, which waited for "O read out" of
+    item k, and the epilogue warps read item k's statistics before they
+    arrive on that.  In the split design (P over S, no P.V wait before P) it
+    is needed, as the planted mistake shows.  The kernel keeps it in both."""
     for seed in range(150):
-        simulate(128, seed, mut="no_ofree")
-        simulate(64, seed, mut="one_xch_slot")
+        simulate(128, seed, mut="no_stfree")
