@@ -37,11 +37,10 @@
 //              stores at all: their barriers (bar.sync, mbarrier arrive with
 //              release semantics) would otherwise wait for those stores to
 //              complete, a long stall at every item boundary.
-//   warp 12    TMA producer: Q once per item, K_j / V_j into rings of stages,
-//              K two tiles ahead of V.
+//   warp 12    TMA producer of Q (once per item) and K_j (a ring of stages).
 //   warp 13    score MMA issuer (S_j = Q K_j^T); also allocates TMEM.
 //   warp 14    P.V MMA issuer.
-//   warp 15    idle (it completes the fourth warpgroup of the register split).
+//   warp 15    TMA producer of V_j (a ring of stages).
 //   The issuers are converged warps; one elected lane issues each copy, MMA
 //   and commit.  Two MMA issuers on two sub-partitions halve the instruction
 //   stream each must get through per tile while the softmax warps' exponent
@@ -113,7 +112,8 @@ constexpr int EPI_WARPS = 4;
 constexpr int WARP_TMA = 12;
 constexpr int WARP_MMA_S = 13;
 constexpr int WARP_MMA_O = 14;
-constexpr int NUM_THREADS = 16 * 32;  // warp 15 only completes the fourth warpgroup
+constexpr int WARP_TMA_V = 15;
+constexpr int NUM_THREADS = 16 * 32;
 // Registers a thread after the split (launched with 65536 / 512 = 128): the
 // softmax warpgroups take 168, the other two 88; 256 * (168 + 88) = 65536.
 constexpr uint32_t REGS_SOFTMAX = 168;
@@ -212,7 +212,7 @@ struct Layout {
     static constexpr int B_OFREE = B_OFINAL + 1;
     static constexpr int B_DRAIN = B_OFREE + 1;  // 2 (one per MMA issuer)
     static constexpr int B_STFULL = B_DRAIN + 2;  // 2 (per stats slot): the softmax warps wrote it
-    static constexpr int B_STFREE = B_STFULL + 2; // 2 (per stats slot): the epilogue warps read it
+    static constexpr int B_STFREE = B_STFULL + 2; // 2 (per stats slot): the epilogue warps read it (split design)
     static constexpr int NUM_BARS = B_STFREE + 2;
     static constexpr uint32_t OFF_MISC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // [0] TMEM base, [1] abort
     // The dynamic shared memory base is 1024-byte aligned (no static shared
@@ -525,8 +525,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_TMA && lane == 0) {
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
-        ptx::prefetch_tensormap(&tm_v);
     }
+    if (warp == WARP_TMA_V && lane == 0) ptx::prefetch_tensormap(&tm_v);
     if (warp == WARP_MMA_S) {
         ptx::tmem_alloc(sbase + L::OFF_MISC, TM_COLS);
         ptx::tmem_relinquish();
@@ -540,43 +540,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp >= SOFTMAX_WARPS) {
         ptx::setmaxnreg_dec<REGS_OTHER>();
         if (warp == WARP_TMA) {
-            // ------------------------------------------------------ TMA producer
+            // ------------------------------------------- TMA producer: Q and K
             // The whole warp runs the loop (warp-uniform control flow, so the
             // compiler keeps its bookkeeping on the uniform datapath); one elected
-            // lane issues each copy.  K of global tile g is issued, then V of tile
-            // g-2 of the same item: the score MMA needs K a whole softmax step
-            // before the P.V MMA needs V.  The (head, key tile) of the last three
-            // K tiles are remembered for V.
-            int gk = 0, gv = 0;
-            int vb0 = 0, vb1 = 0, vb2 = 0, vj0 = 0, vj1 = 0, vj2 = 0;
+            // lane issues each copy: K of every tile as soon as its stage is
+            // free, and an item's Q after the item's first K tile, as soon as
+            // every score MMA of the item before is done (a K stage frees up
+            // a few tiles earlier than Q).  V has a producer of its own
+            // (below), so the loads the score stream needs never queue behind
+            // a wait for a P.V.
+            int gk = 0;
             bool ok = true;
-            auto remember = [&](int g, int bh, int j) {
-                const int r = g % 3;
-                vb0 = (r == 0) ? bh : vb0;
-                vj0 = (r == 0) ? j : vj0;
-                vb1 = (r == 1) ? bh : vb1;
-                vj1 = (r == 1) ? j : vj1;
-                vb2 = (r == 2) ? bh : vb2;
-                vj2 = (r == 2) ? j : vj2;
-            };
-            auto issue_v = [&]() -> bool {
-                const int s = gv % L::VSTAGES;
-                const uint32_t ph = (uint32_t)(gv / L::VSTAGES) & 1u;
-                if (!warp_wait_bar(bar(L::B_VEMPTY + s), ph ^ 1u, limit, abort_flag, 0x100 + L::B_VEMPTY + s))
-                    return false;
-                const int r = gv % 3;
-                const int vbh = (r == 0) ? vb0 : ((r == 1) ? vb1 : vb2);
-                const int vj = (r == 0) ? vj0 : ((r == 1) ? vj1 : vj2);
-                if (ptx::elect_one()) {
-                    ptx::mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::KV_BYTES);
-                    FA_TRACE_EV(WARP_TMA, gv, 1);
-                    for (int c = 0; c < L::DBLK; ++c)
-                        ptx::tma_load_3d(sbase + L::OFF_V + s * L::VSTAGE + c * BLK_BYTES, &tm_v,
-                                         bar(L::B_VFULL + s), c * 64, vj * BN, vbh);
-                }
-                ++gv;
-                return true;
-            };
             // Q of item i, the nq-th Q load, once every score MMA of the item
             // before it is done (Q_EMPTY; the phase before cannot alias: this
             // warp waited for it before the load before).
@@ -596,7 +570,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 return true;
             };
             int i = first_item(), step = 0;
-            if (i < p.num_items) ok = load_q(i);
             while (ok && i < p.num_items) {
                 const Item it = item_of<CAUSAL>(i, p);
                 for (int j = 0; ok && j < it.n_kv; ++j) {
@@ -615,20 +588,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ptx::tma_load_3d(sbase + L::OFF_K + s * L::KV_BYTES + c * BLK_BYTES, &tm_k,
                                              bar(L::B_KFULL + s), c * 64, j * BN, it.bh);
                     }
-                    remember(gk, it.bh, j);
                     ++gk;
-                    if (gv <= gk - 3) ok = issue_v();
+                    if (j == 0) {
+                        ok = load_q(i);
+                        // The next item's Q into L2 now: its load into shared
+                        // memory can start only once this item's last score
+                        // MMA is done, and would otherwise wait on HBM then.
+                        int step_next = step;
+                        const int i_next = next_item(i, step_next);
+                        if (i_next < p.num_items && ptx::elect_one()) {
+                            const Item in = item_of<CAUSAL>(i_next, p);
+                            for (int c = 0; c < L::DBLK; ++c) ptx::tma_prefetch_3d(&tm_q, c * 64, in.q0, in.bh);
+                        }
+                    }
                 }
-                // The next item's Q goes out as soon as this item's last score
-                // MMA is done, ahead of this item's last V loads: the next
-                // item's first score MMAs need it a whole softmax step before
-                // this item's last P.V needs V, and no score MMA waits for V.
-                int step_next = step;
-                const int i_next = next_item(i, step_next);
-                if (ok && i_next < p.num_items) ok = load_q(i_next);
-                while (ok && gv < gk) ok = issue_v();
-                i = i_next;
-                step = step_next;
+                i = next_item(i, step);
             }
             // Drain: every copy this warp issued must land before exit.
             if (nq > 0) drain_bar(bar(L::B_QFULL), (uint32_t)((nq - 1) & 1), limit, abort_flag, 0x180);
@@ -636,6 +610,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!(g == p.debug_skip_k && blockIdx.x == 0))
                     drain_bar(bar(L::B_KFULL + g % L::KSTAGES), (uint32_t)(g / L::KSTAGES) & 1u, limit,
                               abort_flag, 0x181);
+        } else if (warp == WARP_TMA_V) {
+            // ------------------------------------------------ TMA producer: V
+            // V of every tile as soon as its stage is free, i.e. once the P.V
+            // that read the stage VSTAGES tiles before is complete.
+            int gv = 0;
+            bool ok = true;
+            for (int i = first_item(), step = 0; ok && i < p.num_items; i = next_item(i, step)) {
+                const Item it = item_of<CAUSAL>(i, p);
+                for (int j = 0; ok && j < it.n_kv; ++j) {
+                    const int s = gv % L::VSTAGES;
+                    const uint32_t ph = (uint32_t)(gv / L::VSTAGES) & 1u;
+                    if (!(ok = warp_wait_bar(bar(L::B_VEMPTY + s), ph ^ 1u, limit, abort_flag,
+                                             0x100 + L::B_VEMPTY + s)))
+                        break;
+                    if (ptx::elect_one()) {
+                        ptx::mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::KV_BYTES);
+                        FA_TRACE_EV(WARP_TMA_V, gv, 1);
+                        for (int c = 0; c < L::DBLK; ++c)
+                            ptx::tma_load_3d(sbase + L::OFF_V + s * L::VSTAGE + c * BLK_BYTES, &tm_v,
+                                             bar(L::B_VFULL + s), c * 64, j * BN, it.bh);
+                    }
+                    ++gv;
+                }
+            }
+            // Drain: every copy this warp issued must land before exit.
             for (int g = max(0, gv - L::VSTAGES); g < gv; ++g)
                 drain_bar(bar(L::B_VFULL + g % L::VSTAGES), (uint32_t)(g / L::VSTAGES) & 1u, limit,
                           abort_flag, 0x182);
@@ -863,7 +862,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::reg_fence4(st);
                 ptx::tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_relaxed(bar(L::B_STFREE + slot));
+                // The slot may be written again (the split design waits for
+                // this; at D = 128 the slot's reuse is ordered through O_FREE).
+                if (L::SPLIT && lane == 0) ptx::mbar_arrive_relaxed(bar(L::B_STFREE + slot));
                 // The item's last P.V (the phase before, the previous item's, was
                 // waited for here before O_FREE let this item's first P.V start).
                 if (!(ok = warp_wait_bar(bar(L::B_OFINAL), (uint32_t)(kitem & 1), limit, abort_flag,
@@ -1277,10 +1278,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         float l_lo, l_hi;
                         ptx::f2_unpack(ptx::f2_add(ptx::f2_add(lsum[0], lsum[1]), ptx::f2_add(lsum[2], lsum[3])), l_lo,
                                        l_hi);
+                        // The slot held item kitem - 2, and its statistics have
+                        // been read: they were read before O_FREE of that item,
+                        // which the first P.V of item kitem - 1 waited for, and
+                        // every P of this item was written after a P.V of item
+                        // kitem - 1 or later was complete (O_DONE).
                         const int slot = kitem & 1;
-                        if (ok)
-                            ok = warp_wait_bar(bar(L::B_STFREE + slot), ((uint32_t)(kitem >> 1) & 1u) ^ 1u, limit,
-                                               abort_flag, 0x380 + L::B_STFREE + slot);
                         if (ok) {
                             const uint32_t st = tmem + lane_off + TM_ST + 4u * (uint32_t)slot;
                             ptx::tmem_st1(st + (uint32_t)half, __float_as_uint(m_ref));

@@ -131,6 +131,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 // ----------------------------------------------------------------------- TMA
 
 // 3-D tiled bulk copy global -> shared; completion is counted in bytes on `bar`.
+// Prefetch of a tile into L2 (no shared memory, nothing to wait for): a later
+// load of the same tile is then an L2 hit.  The x coordinate obeys the same
+// 16-byte rule as a load; out-of-range parts are ignored.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2)
 {

@@ -225,7 +225,7 @@ class Model:
             self.vc[name] = {name: 1}
         live = dict(roles)
         for _ in range(max_steps):
-            roles_ready = [("role", n) for n in live if self._runnable(n)]
+            roles_ready = [("role", n) for n in sorted(live) if self._runnable(n)]
             engine = [("tc", qn) for qn, qu in self.queues.items() if qu]
             engine += [("tma", i) for i in range(len(self.inflight))]
             engine += [("bulk", i) for i in range(len(self.bulk_pending))]

@@ -43,14 +43,14 @@ def simulate(roles, expected, seed, p_timeout):
     live = set(roles)
     while live:
         choices = []
-        for n in live:
+        for n in sorted(live):  # a fixed order: the schedule depends on the seed alone
             kind, arg = state[n]
             if kind == "ready":
                 choices.append(n)
             elif kind == "wait" and (arg in events or aborted or rng.random() < p_timeout):
                 choices.append(n)
         if not choices:
-            waiting = [n for n in live if state[n][0] == "wait"]
+            waiting = [n for n in sorted(live) if state[n][0] == "wait"]
             if not waiting:
                 raise Deadlock({n: state[n] for n in live})
             choices = waiting  # only a timeout can move on

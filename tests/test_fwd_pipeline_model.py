@@ -1,12 +1,12 @@
 """Happens-before model of the attention-forward kernel's pipeline (CPU only).
 
-fa_fwd_kernel.cuh coordinates a TMA producer warp, a score-MMA issuer, a
-P.V-MMA issuer, eight softmax warps and four epilogue warps through
-mbarriers (waited on by parity), hardware named barriers and the
-asynchronous completion of TMA copies and tcgen05 MMAs.  This test replays every role's sequence of barrier
-operations and buffer accesses in the order the kernel executes them, under
-random interleavings and random completion times of the copies and MMAs, and
-checks:
+fa_fwd_kernel.cuh coordinates two TMA producer warps (Q and K; V), a
+score-MMA issuer, a P.V-MMA issuer, eight softmax warps and four epilogue
+warps through mbarriers (waited on by parity), hardware named barriers and
+the asynchronous completion of TMA copies and tcgen05 MMAs.  This test
+replays every role's sequence of barrier operations and buffer accesses in
+the order the kernel executes them, under random interleavings and random
+completion times of the copies and MMAs, and checks:
 
 * no data race: every two conflicting accesses to a buffer (the Q, K and V
   stages in shared memory; the S, P and O regions of TMEM per lane quarter
@@ -71,42 +71,41 @@ def mbarrier_counts(split):
 # The roles yield the actions listed in _pipeline_model.
 
 
-def producer(items, D, mut):
-    KS, VS = KSTAGES[D], VSTAGES[D]
-    gk = gv = 0
-
-    def issue_v():
-        nonlocal gv
-        s = gv % VS
-        yield ("wait", f"VEMPTY{s}", gv // VS - 1)
-        yield ("tma", f"VFULL{s}", gv // VS, [f"V{s}"])
-        gv += 1
+def producer_qk(items, D, mut):
+    """Warp 12: K of every tile, and an item's Q after its first K tile,
+    once the previous item's last score MMA is done."""
+    KS = KSTAGES[D]
+    gk = 0
 
     def load_q(k):
-        # Q of item k once every score MMA of item k - 1 is done
         yield ("wait", "QEMPTY", k - (2 if mut == "q_early" else 1))
         yield ("tma", "QFULL", k, ["Q"])
 
-    if items:
-        yield from load_q(0)
     for k, n in enumerate(items):
-        for _ in range(n):
+        for j in range(n):
             s = gk % KS
             yield ("wait", f"KEMPTY{s}", gk // KS - (2 if mut == "k_early" else 1))
             yield ("tma", f"KFULL{s}", gk // KS, [f"K{s}"])
             gk += 1
-            if gv <= gk - 3:
-                yield from issue_v()
-        # the next item's Q ahead of this item's last V loads
-        if k + 1 < len(items):
-            yield from load_q(k + 1)
-        while gv < gk:
-            yield from issue_v()
+            if j == 0:
+                yield from load_q(k)
     # drain: every copy lands before the CTA exits
     if items:
         yield ("wait", "QFULL", len(items) - 1)
     for g in range(max(0, gk - KS), gk):
         yield ("wait", f"KFULL{g % KS}", g // KS)
+
+
+def producer_v(items, D, mut):
+    """Warp 15: V of every tile as soon as its stage is free."""
+    VS = VSTAGES[D]
+    gv = 0
+    for n in items:
+        for _ in range(n):
+            s = gv % VS
+            yield ("wait", f"VEMPTY{s}", gv // VS - (2 if mut == "v_early" else 1))
+            yield ("tma", f"VFULL{s}", gv // VS, [f"V{s}"])
+            gv += 1
     for g in range(max(0, gv - VS), gv):
         yield ("wait", f"VFULL{g % VS}", g // VS)
 
@@ -217,7 +216,7 @@ def softmax_warp(w, items, D, split, need, mut):
         # epilogue warps have read what it held two items ago
         one = mut == "one_slot_no_free"
         slot = 0 if one else k & 1
-        if mut != "no_stfree" and not one:
+        if split and mut != "no_stfree" and not one:
             yield ("wait", f"STFREE{slot}", (k >> 1) - 1)
         yield ("wr", f"ST{slot}.{q}.{h}")
         yield ("arrive", f"STFULL{slot}", k if one else k >> 1)
@@ -233,7 +232,8 @@ def epilogue_warp(q, items, split, mut):
         yield ("wait", f"STFULL{slot}", phase)
         yield ("rd", f"ST{slot}.{q}.0")
         yield ("rd", f"ST{slot}.{q}.1")
-        yield ("arrive", f"STFREE{slot}", phase)
+        if split:
+            yield ("arrive", f"STFREE{slot}", phase)
         if mut != "no_ofinal":
             yield ("wait", "OFINAL", k)
         if split:
@@ -255,7 +255,8 @@ def simulate(D, seed, items=None, mut=None):
     keys = range(WARPS) if split else range(4)
     need = {(key, g): rng.random() < p_need for key in keys for g in range(tiles)}
     roles = {
-        "producer": producer(items, D, mut),
+        "producer_qk": producer_qk(items, D, mut),
+        "producer_v": producer_v(items, D, mut),
         "score": score_issuer(items, D, split, mut),
         "pv": pv_issuer(items, D, split, mut),
     }
@@ -291,6 +292,7 @@ MUTANTS = [
     ((128, 64), "no_ofree", "the next item's first P.V overwrites O before the epilogue warps read it"),
     ((128, 64), "no_ofinal", "the epilogue warps read O before the item's last P.V is done"),
     ((128, 64), "k_early", "the producer refills a K stage one phase too early"),
+    ((128, 64), "v_early", "the V producer refills a V stage one phase too early"),
     ((128, 64), "q_early", "the producer loads the next item's Q before the last score MMA read Q"),
     ((64,), "no_stfree", "the softmax warps overwrite a statistics slot before the epilogue read it"),
     ((128, 64), "one_slot_no_free", "one statistics slot, reused without waiting until it has been read"),
@@ -310,13 +312,17 @@ def test_planted_protocol_mistakes_are_caught(designs, mut, what):
         assert caught is not None, f"d = {D}: not caught: {what}"
 
 
-def test_redundant_orderings():
-    """At d = 128 the softmax warps' wait for a free statistics slot is
-    implied by other waits: the statistics of item k + 2 are written after P
-    of item k + 2, whose write waited for a P.V of item k + 1 or later; those
-    P.Vs follow the first P.V of item k + 1, which waited for "O read out" of
-    item k, and the epilogue warps read item k's statistics before they
-    arrive on that.  In the split design (P over S, no P.V wait before P) it
-    is needed, as the planted mistake shows.  The kernel keeps it in both."""
-    for seed in range(150):
-        simulate(128, seed, mut="no_stfree")
+def test_statistics_slot_reuse_at_d128_needs_no_wait():
+    """At d = 128 the kernel writes a statistics slot without waiting for the
+    epilogue warps to have read what it held two items ago: that read is
+    implied.  The statistics of item k + 2 are written after P of item k + 2,
+    whose write waited for a P.V of item k + 1 or later; those P.Vs follow
+    the first P.V of item k + 1, which waited for "O read out" of item k, and
+    the epilogue warps read item k's statistics before they arrive on that.
+    The main tests run the kernel's protocol (no such wait at d = 128); this
+    one runs long item sequences of single tiles, where the statistics turn
+    over fastest.  In the split design (P over S, no P.V wait before a P) the
+    wait is needed, as the planted mistake no_stfree shows."""
+    for seed in range(200):
+        simulate(128, seed, items=[1] * 8)
+        simulate(128, seed, items=[1, 2, 1, 1, 3, 1])
