@@ -77,18 +77,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "739d954fa9f1cd23469ea7127bc3851d2e7a062bb4a0f34237b2bf322031a83a",
-        "bytes": 4 * (201_448_192 + 45_600_000),
+        "sha256": "b939704caade96741cb1f767e8856d2c8d24dc1379677855915a46199348ea46",
+        "bytes": 4 * (201_401_856 + 45_278_976),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "45b03688b85a63656652404595c81e41128253f757bc8a0213092bd1ea3858f0",
-        "bytes": 4 * (406_192_128 + 217_494_272),
+        "sha256": "1f9eb67f4decd48c6e9029f5421d12ea0b4c825390a12a783aa78f6fe4e8d4da",
+        "bytes": 4 * (406_265_088 + 217_518_080),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "f7df67582338d11f98f8d715252075973271aa1bf134ae2a4433edfc6805e5d6",
-        "bytes": 285_242_368 + 210_490_368,
+        "sha256": "326c8f1f7c50d7b5b81f1f91546434947f1381adfbe982b5d16ce36d06708d80",
+        "bytes": 285_239_040 + 210_368_768,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
