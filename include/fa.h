@@ -78,6 +78,11 @@ typedef enum fa_status {
  * been synchronised.  Errors found before the launch are returned directly;
  * a pipeline timeout inside the kernel is reported by fa_check_device_status.
  * o and lse must not overlap q, k, v or each other (FA_ERR_INVALID_ARG).
+ * The kernel is launched as a programmatic dependent of the work before it
+ * on `stream` (CUDA programmatic dependent launch): its blocks may start and
+ * set up while that work's last blocks run, but read and write device memory
+ * only once it has completed, so stream order holds as for a plain launch.
+ * The device is the calling thread's current device.
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int64_t B,
                  int64_t H, int64_t N, int64_t d, int causal, float scale, fa_stream_t stream);
@@ -123,7 +128,8 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
  *   stream   CUDA stream the work is enqueued on.
  *
  * Ownership: the caller allocates every buffer, including the workspace; the
- * library allocates nothing.  Asynchrony as for fa_fwd.  Errors: as fa_fwd,
+ * library allocates nothing.  Asynchrony and launches as for fa_fwd (both
+ * kernels).  Errors: as fa_fwd,
  * plus FA_ERR_INVALID_ARG for a missing or short workspace, and
  * FA_ERR_UNSUPPORTED for Nq > 8 or a workspace that is not 16-byte aligned.
  * The sizes, scale, pointers and overlaps with the inputs are checked before
@@ -243,7 +249,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
  * Ownership: the caller owns every buffer.  x, bias, y 16-byte aligned and
  * keep 4-byte aligned, else FA_ERR_UNSUPPORTED.  y may not overlap x, bias or
  * keep (FA_ERR_INVALID_ARG); x may be y's input only out of place.
- * Asynchrony and FA_ERR_CUDA as for fa_fwd.
+ * Asynchrony, launch and FA_ERR_CUDA as for fa_fwd.
  */
 fa_status fa_bias_gelu_dropout(const void *x, const void *bias, const uint32_t *keep, void *y,
                                int64_t rows, int64_t cols, float p, fa_stream_t stream);

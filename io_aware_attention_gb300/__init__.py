@@ -28,6 +28,10 @@ keep mask drawn by the caller) in one HBM read and one write.
 
 The ``*_into`` forms write into caller-provided tensors; their shapes, dtypes
 and devices are checked here, because the C ABI sees only pointers and sizes.
+Work is enqueued on ``stream``, by default the current stream, of the current
+CUDA device, which must be the tensors' device (``fwd``, ``bwd`` and
+``decode`` switch to it themselves).  The checks of a ``fwd_into`` call take
+one pass over its tensors (a few microseconds of host time per call).
 """
 from __future__ import annotations
 
@@ -111,12 +115,40 @@ def version() -> int:
     return int(library().fa_version())
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device: int | None = None):
+    """The raw cudaStream_t of ``stream`` as an int, else the current stream
+    of ``device`` (default: the current device)."""
     import torch
 
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if device is None:
+        device = torch.cuda.current_device()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return int(raw(device))
+    return int(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _on_current_device(dev: int) -> None:
+    """The C entry points launch on the calling thread's current device, so
+    the tensors must live there."""
+    import torch
+
+    cur = torch.cuda.current_device()
+    if dev != cur:
+        raise ValueError(f"tensors are on cuda:{dev} but the current device is cuda:{cur}: "
+                         f"call under torch.cuda.device({dev})")
+
+
+def _fast_ok(dev: int, shape, dtype, *ts) -> bool:
+    """One pass over tensors that must all be contiguous, of this dtype and
+    shape, on CUDA device dev (the common case; any failure is reported by
+    the detailed checks)."""
+    for t in ts:
+        if t.get_device() != dev or t.dtype is not dtype or t.shape != shape or not t.is_contiguous():
+            return False
+    return True
 
 
 def _check(q, k, v):
@@ -155,16 +187,20 @@ def fwd_into(q, k, v, o, lse, causal: bool = False, scale: float | None = None, 
     ``lse`` (fp32, (B, H, N))."""
     import torch
 
-    _check(q, k, v)
-    B, H, N, d = (int(s) for s in q.shape)
-    _check_out("o", o, q.shape, torch.bfloat16, q.device)
-    _check_out("lse", lse, (B, H, N), torch.float32, q.device)
+    shape = q.shape
+    dev = q.get_device()
+    if not (dev >= 0 and len(shape) == 4 and _fast_ok(dev, shape, torch.bfloat16, q, k, v, o)
+            and lse.get_device() == dev and lse.dtype is torch.float32 and lse.shape == shape[:3]
+            and lse.is_contiguous()):
+        _check(q, k, v)
+        _check_out("o", o, q.shape, torch.bfloat16, q.device)
+        _check_out("lse", lse, tuple(q.shape[:3]), torch.float32, q.device)
+    _on_current_device(dev)
+    B, H, N, d = shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    rc = library().fa_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
-                          ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
-                          ctypes.c_void_p(lse.data_ptr()), B, H, N, d, int(bool(causal)),
-                          float(scale), _stream_handle(stream))
+    rc = library().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                          1 if causal else 0, float(scale), _stream_handle(stream, dev))
     if rc != 0:
         raise FaError(rc, "fa_fwd")
     return o, lse
@@ -211,11 +247,13 @@ def bwd_into(q, k, v, o, lse, do, dq, dk, dv, workspace, causal: bool = False, s
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     ws_bytes = workspace.numel() * workspace.element_size()
+    dev = q.get_device()
+    _on_current_device(dev)
     vp = ctypes.c_void_p
     rc = library().fa_bwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(o.data_ptr()),
                           vp(lse.data_ptr()), vp(do.data_ptr()), vp(dq.data_ptr()), vp(dk.data_ptr()),
                           vp(dv.data_ptr()), B, H, N, d, int(bool(causal)), float(scale), vp(workspace.data_ptr()),
-                          ws_bytes, _stream_handle(stream))
+                          ws_bytes, _stream_handle(stream, dev))
     if rc != 0:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
@@ -256,11 +294,13 @@ def bias_gelu_dropout(x, bias, keep=None, p: float = 0.0, out=None, stream=None)
         raise ValueError("x, bias and keep must be on one device")
     if out is not None:
         _check_out("out", out, x.shape, torch.bfloat16, x.device)
+    dev = x.get_device()
+    _on_current_device(dev)
     y = torch.empty_like(x) if out is None else out
     vp = ctypes.c_void_p
     rc = library().fa_bias_gelu_dropout(vp(x.data_ptr()), vp(bias.data_ptr()),
                                         vp(keep.data_ptr() if keep is not None else 0), vp(y.data_ptr()), rows,
-                                        cols, float(p), _stream_handle(stream))
+                                        cols, float(p), _stream_handle(stream, dev))
     if rc != 0:
         raise FaError(rc, "fa_bias_gelu_dropout")
     return y
@@ -304,12 +344,14 @@ def decode_into(q, k, v, o, lse, workspace, causal: bool = False, scale: float |
         raise ValueError("workspace must be a contiguous CUDA tensor on the inputs' device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    dev = q.get_device()
+    _on_current_device(dev)
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else ctypes.c_void_p(0)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = library().fa_decode(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
                              ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(o.data_ptr()),
                              ctypes.c_void_p(lse.data_ptr()), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
-                             ws_ptr, ws_bytes, _stream_handle(stream))
+                             ws_ptr, ws_bytes, _stream_handle(stream, dev))
     if rc != 0:
         raise FaError(rc, "fa_decode")
     return o, lse

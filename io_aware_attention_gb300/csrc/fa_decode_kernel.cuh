@@ -31,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "ptx.cuh"
+
 namespace fa {
 namespace dec {
 
@@ -99,6 +101,8 @@ template <int D, int QM, bool PAD>
 __global__ void __launch_bounds__(THREADS)
     fa_decode_partial_kernel(const Params p)
 {
+    ptx::griddep_wait();  // a programmatic dependent: the inputs are complete
+    ptx::griddep_launch_dependents();
     using C = Cfg<D, QM>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = lane / C::G, sub = lane % C::G;  // key of the load, 8 columns of it
@@ -263,6 +267,8 @@ __global__ void __launch_bounds__(THREADS)
 template <int D>
 __global__ void __launch_bounds__(D) fa_decode_combine_kernel(const Params p)
 {
+    ptx::griddep_wait();  // a programmatic dependent: the partial results are complete
+    ptx::griddep_launch_dependents();
     const int64_t row = blockIdx.x;  // (bh, query)
     const int c = threadIdx.x;
     const int dd = p.d;

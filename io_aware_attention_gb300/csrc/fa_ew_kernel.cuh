@@ -108,6 +108,8 @@ __device__ __forceinline__ uint32_t chain2(uint32_t xw, uint32_t bw, uint64_t fa
 template <bool WIDE>
 __global__ void __launch_bounds__(THREADS, 4) fa_bias_gelu_dropout_kernel(const Params p)
 {
+    ptx::griddep_wait();  // a programmatic dependent: the inputs are complete
+    ptx::griddep_launch_dependents();
     // Dropout factors of an element pair, indexed by its two keep bits.
     __shared__ uint64_t ftab[4];
     if (threadIdx.x < 4)

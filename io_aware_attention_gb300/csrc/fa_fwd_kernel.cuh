@@ -535,6 +535,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem = misc[0];
+    // Launched as a programmatic dependent of the kernel before it on the
+    // stream: the set-up above overlapped that kernel's last blocks; global
+    // memory is touched only after it has completed.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     // Warpgroups 2-3 give up registers that warpgroups 0-1 (the softmax
     // warps) take; each register change heads the code of its warpgroups.
     if (warp >= SOFTMAX_WARPS) {

@@ -576,5 +576,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this one
+// depends on have completed and their memory operations are visible (at
+// once when it was launched without a programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid on the stream start launching once every block of this
+// one has said so or exited; its blocks then set up and wait in
+// griddep_wait for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 }  // namespace ptx
 }  // namespace fa
