@@ -77,18 +77,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "b939704caade96741cb1f767e8856d2c8d24dc1379677855915a46199348ea46",
-        "bytes": 4 * (201_401_856 + 45_278_976),
+        "sha256": "4483623b9fcf12d2a12db1642e6813a7bdd08cea1f917823f08d3bd1f0d32f18",
+        "bytes": 4 * (201_404_672 + 45_226_240),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "1f9eb67f4decd48c6e9029f5421d12ea0b4c825390a12a783aa78f6fe4e8d4da",
-        "bytes": 4 * (406_265_088 + 217_518_080),
+        "sha256": "c3a83060313d581a9a024f5ef28a10274e271a06eef3c77a023e7bdc48095c79",
+        "bytes": 4 * (406_624_000 + 217_467_392),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "326c8f1f7c50d7b5b81f1f91546434947f1381adfbe982b5d16ce36d06708d80",
-        "bytes": 285_239_040 + 210_368_768,
+        "sha256": "be8405ea4fa8c3ab42e6536ab248e5db70a8069c8869a4c2afbad20928b9bc55",
+        "bytes": 285_241_344 + 210_531_072,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
