@@ -77,18 +77,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "4483623b9fcf12d2a12db1642e6813a7bdd08cea1f917823f08d3bd1f0d32f18",
-        "bytes": 4 * (201_404_672 + 45_226_240),
+        "sha256": "607ea0b96f57e5f5e67d68e0e97446a34c34b1c6b1d3b047f32918e50661fe78",
+        "bytes": 4 * (201_418_752 + 45_513_984),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "c3a83060313d581a9a024f5ef28a10274e271a06eef3c77a023e7bdc48095c79",
-        "bytes": 4 * (406_624_000 + 217_467_392),
+        "sha256": "1128aa0c6766f8853a73a09761f166f2812c0f742477e9f1478653d41d3aea73",
+        "bytes": 4 * (406_800_384 + 218_594_816),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "be8405ea4fa8c3ab42e6536ab248e5db70a8069c8869a4c2afbad20928b9bc55",
-        "bytes": 285_241_344 + 210_531_072,
+        "sha256": "b63cd7396eebb754f8525ef3730603a73fe834ddcd7860e19028c9f0eff142f2",
+        "bytes": 285_238_784 + 210_507_008,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

@@ -26,8 +26,9 @@
 //              lane quarter) and score columns 64*(w/4) .. +63, so every SM
 //              sub-partition runs two softmax warps (w and w+4, the two halves
 //              of the same rows).  Each thread owns half a row: masking,
-//              partial row max (exchanged with the partner warp through TMEM
-//              and a 64-thread named barrier), exponentials, its half of
+//              partial row max (returned with the scores by the TMEM load
+//              itself, tcgen05.ld.red, and exchanged with the partner warp
+//              through TMEM and a 64-thread named barrier), exponentials, its half of
 //              P and its half of the O columns for rescaling.  At the end of
 //              an item it leaves its reference max and row sum in TMEM for
 //              the epilogue warps and goes straight on to the next item.
@@ -1025,9 +1026,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::named_barrier_sync(nb_sready + (uint32_t)(g % 3), NB_SREADY_SPLIT_COUNT);
                         if (!ok) continue;
                         ptx::tc_fence_after_sync();
-                        ptx::tmem_ld64(s_half, sr);
+                        // The load also returns the max of the 64 scores (the TMEM
+                        // load's reduction); a masked tile takes it again after the
+                        // mask.
+                        float red;
+                        ptx::tmem_ld64_max(s_half, sr, red);
                         if (lane == 0) FA_TRACE_EV(warp, g, 0);
-                        ptx::tmem_wait_ld64(sr);
+                        ptx::tmem_wait_ld64_max(sr, red);
                         if (lane == 0) FA_TRACE_EV(warp, g, 1);
                         // Causal diagonal tile / keys past N: -inf before the max.
                         const int k0 = j * BN + half * 64;
@@ -1035,8 +1040,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     #pragma unroll
                             for (int c = 0; c < 64; ++c)
                                 if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
+                            red = max64(sr);
                         }
-                        const float m_tile = max64(sr) * sl2;  // scale > 0, so max commutes with it
+                        const float m_tile = red * sl2;  // scale > 0, so max commutes with it
                         if (lane == 0) FA_TRACE_EV(warp, g, 2);
 
                         // A half-row may have no visible key yet (its reference then
@@ -1164,14 +1170,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int b = g & 1;
                         // S of tile g is in TMEM (met on every tile, also after an abort).
                         ptx::named_barrier_sync(NB_SREADY0 + (uint32_t)(g % 3), NB_SREADY_COUNT);
+                        // The load also returns the max of the 64 scores (the TMEM
+                        // load's reduction); a masked tile takes it again after the
+                        // mask.
+                        float red = -INFINITY;
                         if (ok) {
                             ptx::tc_fence_after_sync();
-                            ptx::tmem_ld64(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr);
+                            ptx::tmem_ld64_max(tmem + lane_off + (b ? TM_S1 : TM_S0) + (uint32_t)half * 64, sr, red);
                         }
                         if (lane == 0) FA_TRACE_EV(warp, g, 0);
                         float mx = -INFINITY;
                         if (ok) {
-                            ptx::tmem_wait_ld64(sr);
+                            ptx::tmem_wait_ld64_max(sr, red);
                             // The scores are in registers: S of tile g + 2 may now be
                             // written into this buffer.
                             ptx::tc_fence_before_sync();
@@ -1184,8 +1194,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     #pragma unroll
                                 for (int c = 0; c < 64; ++c)
                                     if (k0 + c > key_max) sr[c] = __float_as_uint(-INFINITY);
+                                mx = max64(sr);
+                            } else {
+                                mx = red;
                             }
-                            mx = max64(sr);
                             ptx::tmem_st1(tmem + lane_off + TM_MX + (uint32_t)(b * 2 + half), __float_as_uint(mx));
                             ptx::tmem_wait_st();
                             ptx::tc_fence_before_sync();
