@@ -114,3 +114,25 @@ def test_python_checks_reject_bad_tensors():
         # head sizes must be multiples of 8 (up to 128)
         fa.fwd(q[..., :36].contiguous(), k[..., :36].contiguous(), v[..., :36].contiguous())
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("pos", [0, 1, 31, 63, 64, 65, 96, 127])
+def test_row_max_at_each_column(pos, causal, d):
+    """The row max of a tile comes back with the TMEM load of the scores; put
+    it on a chosen key column of every tile (the first and last of each
+    64-column half among them) by scaling that key up, with a tie in the
+    other half, and compare with the oracle.  The planted keys dominate their
+    rows, so O comes close to single value rows; V is halved (exactly, in
+    bf16) so that |O| stays where the bf16 rounding of the output (half an
+    ulp: 2^-8 |O|) is within the absolute tolerance."""
+    N = 640
+    q, k, v = make_random_qkv(1, 2, N, d, seed=300 + pos + d)
+    k, v = k.clone(), v * 0.5
+    k[:, :, pos::128] *= 6
+    k[:, :, (pos + 64) % 128::128] = k[:, :, pos::128][:, :, : k[:, :, (pos + 64) % 128::128].shape[2]]
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_guarded(q.cuda(), k.cuda(), v.cuda(), causal, scale)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal, scale)
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"max at column {pos}")
