@@ -77,13 +77,13 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "607ea0b96f57e5f5e67d68e0e97446a34c34b1c6b1d3b047f32918e50661fe78",
-        "bytes": 4 * (201_418_752 + 45_513_984),
+        "sha256": "b96eba35e10a5909bcccebb5dc216890e0fe98ec6a361449d2a7036502776cde",
+        "bytes": 4 * (201_461_248 + 45_022_976),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "1128aa0c6766f8853a73a09761f166f2812c0f742477e9f1478653d41d3aea73",
-        "bytes": 4 * (406_800_384 + 218_594_816),
+        "sha256": "90da0681e1e8cee8c28f6acd623701cc96187b86c16a1f6281d00d5b8bc8d646",
+        "bytes": 4 * (406_646_016 + 217_909_760),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,

@@ -46,8 +46,9 @@
 //   and commit.  Two MMA issuers on two sub-partitions halve the instruction
 //   stream each must get through per tile while the softmax warps' exponent
 //   loops take most of the issue slots.  Registers: the CTA is launched with
-//   128 a thread; the two softmax warpgroups raise theirs to 168 and the other
-//   two lower theirs to 88 (setmaxnreg), which adds up to the register file.
+//   128 a thread; the two softmax warpgroups raise theirs to 168 (D = 128;
+//   152 at D = 64) and the other two lower theirs to 88 (104) (setmaxnreg),
+//   which adds up to the register file.
 //
 // TMEM columns (512 allocated, lanes = query rows):
 //   [  0,128) S buffer 0     [128,256) S buffer 1   (fp32 scores, double-buffered)
@@ -116,11 +117,10 @@ constexpr int WARP_MMA_O = 14;
 constexpr int WARP_TMA_V = 15;
 constexpr int NUM_THREADS = 16 * 32;
 // Registers a thread after the split (launched with 65536 / 512 = 128): the
-// softmax warpgroups take 168, the other two 88; 256 * (168 + 88) = 65536.
-constexpr uint32_t REGS_SOFTMAX = 168;
-constexpr uint32_t REGS_OTHER = 88;
-static_assert(SOFTMAX_THREADS * REGS_SOFTMAX + (NUM_THREADS - SOFTMAX_THREADS) * REGS_OTHER <= 65536,
-              "register split");
+// softmax warpgroups take REGS_SOFTMAX, the other two REGS_OTHER (per head
+// size, in Layout): 168 / 88 at D = 128, 152 / 104 at D = 64, where the
+// epilogue warps hold a whole row of the split design and the softmax needs
+// fewer; 256 * (168 + 88) = 256 * (152 + 104) = 65536.
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr uint32_t WAIT_SLEEP_NS = 20000;  // suspend-time hint of one poll
 constexpr uint32_t TM_S0 = 0, TM_S1 = 128, TM_O = 256, TM_P = 400, TM_MX = 468, TM_ST = 472;
@@ -184,6 +184,10 @@ struct Layout {
     // separate softmax states and accumulators [O_h | l~_h] (TMEM has room
     // for both at D = 64) and merge them in the epilogue.
     static constexpr bool SPLIT = D == 64;
+    static constexpr uint32_t REGS_SOFTMAX = (D == 64) ? 152 : 168;
+    static constexpr uint32_t REGS_OTHER = (D == 64) ? 104 : 88;
+    static_assert(SOFTMAX_THREADS * REGS_SOFTMAX + (NUM_THREADS - SOFTMAX_THREADS) * REGS_OTHER <= 65536,
+                  "register split");
     static constexpr uint32_t O_STRIDE = D + 16;  // split design: O_1 follows [O_0 | l~_0]
     static constexpr int KSTAGES = (D == 128) ? 3 : 4;  // K runs two tiles ahead of V
     static constexpr int VSTAGES = (D == 128) ? 2 : 4;
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Warpgroups 2-3 give up registers that warpgroups 0-1 (the softmax
     // warps) take; each register change heads the code of its warpgroups.
     if (warp >= SOFTMAX_WARPS) {
-        ptx::setmaxnreg_dec<REGS_OTHER>();
+        ptx::setmaxnreg_dec<L::REGS_OTHER>();
         if (warp == WARP_TMA) {
             // ------------------------------------------- TMA producer: Q and K
             // The whole warp runs the loop (warp-uniform control flow, so the
@@ -908,6 +912,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     fmaf(__uint_as_float(oa[2 * c]), c0, __uint_as_float(ob[2 * c]) * c1),
                                     fmaf(__uint_as_float(oa[2 * c + 1]), c0, __uint_as_float(ob[2 * c + 1]) * c1));
                         }
+                        // The whole row is in registers (the loads above have
+                        // completed): O is released to the next item's first P.V
+                        // before the stores.
+                        ptx::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_relaxed(bar(L::B_OFREE));
                         const int row0 = it.q0 + quarter * 32;
                         store_rows_coalesced(w, p.o + ((int64_t)it.bh * N + row0) * D, lane, N - row0, D);
                     } else {
@@ -977,15 +987,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 // O has been read (every load above has completed): the next
-                // item's first P.V may overwrite it.
-                ptx::tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_relaxed(bar(L::B_OFREE));
+                // item's first P.V may overwrite it.  (The split design's
+                // unpadded path released it before its stores.  At D = 128 the
+                // stores come first: released earlier, they ran beside the next
+                // item's MMAs and slowed them more than the wait costs.)
+                if constexpr (!(L::SPLIT && !PAD)) {
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_relaxed(bar(L::B_OFREE));
+                }
                 if (row_ok) p.lse[(int64_t)it.bh * N + q_idx] = (m + ptx::lg2(l)) * 0.69314718055994530942f;
             }
         }
     } else {
-        ptx::setmaxnreg_inc<REGS_SOFTMAX>();
+        ptx::setmaxnreg_inc<L::REGS_SOFTMAX>();
             if constexpr (L::SPLIT) {
                 // ------------------------------------- softmax warps, split design
                 // Warp w serves query rows 32*(w%4) .. +31 (its TMEM lane quarter) and
