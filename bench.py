@@ -391,16 +391,33 @@ def tensor_roofline(w, flops: float, ms_per_step: float, peaks, peak_src, clocks
     peak = float(peaks["bf16_tflops"])
     tensor_ms = flops / (peak * 1e12) * 1e3
     mufu = mufu_bound(w, ms_per_step, clocks.get("sm_mhz") if clocks else None, sms)
+    executed = executed_flops(w)
     roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "peak_source": f"bf16_tflops (burst), {peak_src}",
             "frac_of_sustained": round(achieved / float(peaks.get("bf16_tflops_sustained", peak)), 4),
             "frac_of_datasheet": round(achieved / DATASHEET_BF16_TFLOPS, 4),
             "datasheet_tflops": DATASHEET_BF16_TFLOPS, "kernel": kernel, "alg_flops_per_launch": flops,
+            "executed_flops_per_launch": executed, "executed_over_algorithmic": round(executed / flops, 4),
+            "executed_frac": round(executed / (ms_per_step * 1e-3) / 1e12 / peak, 4),
             "tensor_bound_ms": round(tensor_ms, 5), "mufu": mufu}
     if mufu:
         roof["binding"] = "tensor" if tensor_ms >= mufu["bound_ms"] else "mufu"
         roof["frac_of_binding"] = round(max(tensor_ms, mufu["bound_ms"]) / ms_per_step, 4)
     return roof
+
+
+def executed_flops(w) -> float:
+    """The tensor work the forward kernel executes per launch, beside the
+    algorithmic 4·B·H·N²·d (halved when causal): whole 128 × 128 tiles
+    (the causal diagonal ones and a ragged tail included) at the kernel's
+    head size D (64 or 128; smaller d are zero-padded), and the P·V product
+    at N = D + 16 (the ones block that makes l~).  Per tile 2·128²·D for S
+    and 2·128²·(D + 16) for P·V; per head M² tiles, or M(M + 1)/2 under the
+    causal mask, M = ceil(N / 128)."""
+    D = 64 if w.d <= 64 else 128
+    M = (w.N + 127) // 128
+    tiles = M * (M + 1) // 2 if w.causal else M * M
+    return float(w.B * w.H * tiles * 2 * 128 * 128 * (2 * D + 16))
 
 
 def fwd_kernel_name(w) -> str:

@@ -57,3 +57,22 @@ def test_binding_bound_switches_with_the_clock():
     slow = bench.tensor_roofline(w, flops, 5.0, PEAKS, "measured", {"sm_mhz": 1000.0}, 152, "k")
     assert fast["binding"] == "tensor" and slow["binding"] == "mufu"
     assert slow["frac_of_binding"] == pytest.approx(slow["mufu"]["bound_ms"] / 5.0, abs=1e-3)
+
+
+def test_executed_tensor_work():
+    """The forward executes whole tiles and the l~ columns: at the headline
+    (d = 128, N = 4096 causal) 1 + 8/128 for the ones block times 33/32 for
+    the diagonal tiles over the algorithmic count; non-causal d = 64 only the
+    ones block (1 + 8/64); a padded head size counts the padded columns."""
+    w = WORKLOADS["b8_h32_n4096_d128_causal"]
+    flops = iomodel.attention_flops(w.B, w.H, w.N, w.d, w.causal)
+    assert bench.executed_flops(w) / flops == pytest.approx((1 + 8 / 128) * 33 / 32, rel=1e-12)
+    w64 = WORKLOADS["b16_h16_n8192_d64_spiky"]
+    assert bench.executed_flops(w64) / iomodel.attention_flops(w64.B, w64.H, w64.N, w64.d, w64.causal) == \
+        pytest.approx(1 + 8 / 64, rel=1e-12)
+    from io_aware_attention_gb300.workloads import Workload
+    w40 = Workload("d40", 1, 1, 256, 40, False, 1)
+    assert bench.executed_flops(w40) == 1 * 1 * 4 * 2 * 128 * 128 * (2 * 64 + 16)
+    roof = bench.tensor_roofline(w, flops, 0.8, PEAKS, "measured", {"sm_mhz": 2070.0}, 152, "k")
+    assert roof["executed_over_algorithmic"] == pytest.approx(1.0957, abs=1e-4)
+    assert roof["executed_frac"] == pytest.approx(bench.executed_flops(w) / 0.8e-3 / 1e12 / 1888.1, abs=1e-4)
