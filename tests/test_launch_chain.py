@@ -160,3 +160,47 @@ def test_forward_backward_forward():
             assert ((a - b).abs() <= 2.0 ** -6 * b.abs() + 1e-3).all(), f"{name} differs from the synchronised chain"
         else:
             assert torch.equal(a, b), f"{name} differs from the synchronised chain"
+
+
+def test_concurrent_streams_and_host_threads():
+    """Two host threads, each on its own stream with its own inputs, call the
+    forward and the decode in a loop at the same time (the tensor-map cache
+    is per host thread, the device status word shared): every result equals
+    the same call made alone."""
+    import threading
+
+    shapes = [(2, 8, 2048, 128, True, 32000), (4, 4, 1000, 64, False, 33000)]
+    data, ref = [], []
+    for B, H, N, d, causal, seed in shapes:
+        q, k, v = (t.cuda() for t in make_random_qkv(B, H, N, d, seed))
+        data.append((q, k, v, causal))
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        od, ld = fa.decode(q[:, :, -2:].contiguous(), k, v, causal=True)
+        ref.append((o, lse, od, ld))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(idx):
+        try:
+            q, k, v, causal = data[idx]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                qd = q[:, :, -2:].contiguous()
+                for _ in range(20):
+                    o, lse = fa.fwd(q, k, v, causal=causal)
+                    od, ld = fa.decode(qd, k, v, causal=True)
+                s.synchronize()
+            r = ref[idx]
+            if not (torch.equal(o, r[0]) and torch.equal(lse, r[1]) and torch.equal(od, r[2]) and torch.equal(ld, r[3])):
+                errors.append(f"thread {idx}: results differ")
+        except Exception as e:  # reported below
+            errors.append(f"thread {idx}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert fa.check_device_status() == 0
