@@ -190,3 +190,20 @@ def test_bwd_full_size_sampled_heads(B, H, N, causal, heads):
     for t in (dq, dk, dv):
         assert torch.isfinite(t).all()
     check_heads(q, k, v, do, causal, 128 ** -0.5, dq, dk, dv, heads, f"B={B} H={H} N={N}")
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_short_heads(d, causal):
+    """1024 heads of 65 rows: every item is one key block of two query steps,
+    so each CTA turns items over every other step (the dK / dV read-out and
+    the item barriers at their fastest).  64 heads, the first and last among
+    them, against the oracle."""
+    B, H, N = 16, 64, 65
+    q, k, v = (t.cuda() for t in make_random_qkv(B, H, N, d, 9900 + d + int(causal)))
+    do = make_random_qkv(B, H, N, d, 9950 + d + int(causal))[0].cuda()
+    scale = d ** -0.5
+    dq, dk, dv = run_bwd(q, k, v, do, causal, scale)
+    rng = np.random.default_rng(9900 + d)
+    heads = sorted({0, B * H - 1, *rng.integers(0, B * H, size=62).tolist()})
+    check_heads(q, k, v, do, causal, scale, dq, dk, dv, heads, f"{B * H} heads of N={N}")
