@@ -315,6 +315,20 @@ fa_status fa_debug_skip_k_tile(int tile);
  */
 fa_status fa_debug_set_schedule(int order);
 
+/*
+ * fa_debug_decode_plan — test hook: the split plan fa_decode would use for
+ * these sizes if `wave` CTAs of its partial kernel were resident at once (on
+ * a device, wave = resident CTAs per SM x SMs).  Host arithmetic only: no
+ * device call.  Writes the number of chunks the key range is cut into
+ * (*splits; 1 = not split) and the keys per chunk (*chunk, the last chunk
+ * may be shorter).  The plan weighs a whole number of waves of equal chunks
+ * against the partial results that splitting adds.
+ * FA_ERR_INVALID_ARG for null outputs, wave < 1 or sizes fa_decode refuses
+ * as invalid; FA_ERR_UNSUPPORTED as fa_decode reports it.
+ */
+fa_status fa_debug_decode_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t wave,
+                               int *splits, int *chunk);
+
 /* Static description of a status code (never NULL). */
 const char *fa_status_string(fa_status s);
 

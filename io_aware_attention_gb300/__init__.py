@@ -47,7 +47,8 @@ __all__ = ["fwd", "fwd_into", "bwd", "bwd_into", "bwd_workspace_bytes", "bias_ge
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA",
           4: "FA_ERR_TIMEOUT", 5: "FA_ERR_TOO_LARGE"}
 EXPORTS = ["fa_fwd", "fa_bwd", "fa_bwd_workspace_bytes", "fa_bias_gelu_dropout", "fa_decode", "fa_decode_workspace_bytes", "fa_decode_static", "fa_check_device_status", "fa_get_device_status",
-           "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_debug_set_schedule", "fa_status_string", "fa_version"]
+           "fa_set_wait_limit_ns", "fa_debug_skip_k_tile", "fa_debug_set_schedule", "fa_debug_decode_plan", "fa_status_string",
+           "fa_version"]
 
 
 class FaError(RuntimeError):
@@ -103,6 +104,9 @@ def library():
     lib.fa_debug_skip_k_tile.restype = ctypes.c_int
     lib.fa_debug_set_schedule.argtypes = [ctypes.c_int]
     lib.fa_debug_set_schedule.restype = ctypes.c_int
+    lib.fa_debug_decode_plan.argtypes = [i64, i64, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int)]
+    lib.fa_debug_decode_plan.restype = ctypes.c_int
     lib.fa_status_string.argtypes = [ctypes.c_int]
     lib.fa_status_string.restype = ctypes.c_char_p
     lib.fa_version.argtypes = []
@@ -409,3 +413,14 @@ def debug_set_schedule(order: int) -> None:
     rc = library().fa_debug_set_schedule(int(order))
     if rc != 0:
         raise FaError(rc, "fa_debug_set_schedule")
+
+
+def debug_decode_plan(B: int, H: int, Nq: int, Nk: int, d: int, wave: int) -> tuple[int, int]:
+    """Test hook: the (splits, keys per chunk) that fa_decode would use if
+    ``wave`` CTAs of its partial kernel were resident at once (host
+    arithmetic only; see fa_debug_decode_plan in include/fa.h)."""
+    splits, chunk = ctypes.c_int(0), ctypes.c_int(0)
+    rc = library().fa_debug_decode_plan(B, H, Nq, Nk, d, wave, ctypes.byref(splits), ctypes.byref(chunk))
+    if rc != 0:
+        raise FaError(rc, "fa_debug_decode_plan")
+    return splits.value, chunk.value

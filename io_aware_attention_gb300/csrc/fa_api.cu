@@ -303,22 +303,47 @@ struct DecodePlan {
     size_t ws_bytes;  // 0 when splits == 1 (the partial kernel writes the output)
 };
 
-// Splits of the key range: about 8 CTAs per SM over all heads (many short
-// waves, a small tail), each CTA streaming at least 4 rounds of keys.  A
-// round is what the kernel instance for head size Dp (64 or 128) takes in
-// one pass; the workspace holds d columns per partial output.
-DecodePlan decode_plan(int64_t BH, int64_t nq, int64_t nk, int64_t d, int sms)
+// Splits of the key range.  Each CTA of the partial kernel streams one chunk
+// (a whole number of rounds, at least 4) of one head's keys, and `wave` CTAs
+// are resident at once.  All chunks cost about the same, so the cache is read
+// in about (waves) x (chunk) time, waves = ceil(CTAs / wave): a last wave
+// holding a few CTAs costs a whole chunk while most of the GPU idles.  Split
+// results add traffic: the partial outputs are written and read back once.
+// In bytes at the full bandwidth:
+//   cost = waves * chunk * (K and V bytes a key) * wave + 2 * (partials' bytes).
+// Candidates: 1 to 16 splits, and for k = 1 .. 8 the most splits that fill k
+// waves.  The plan takes the candidate of least cost, or the smallest one
+// within 2% of it.  A round is what the kernel instance for head size Dp
+// (64 or 128) takes in one pass; the workspace holds d columns per partial
+// output.
+DecodePlan decode_plan(int64_t BH, int64_t nq, int64_t nk, int64_t d, int64_t wave)
 {
     DecodePlan pl;
     pl.slots = decode_slots(nq);
     const int64_t Dp = padded_head_size(d);
-    const int round = fa::dec::WARPS * fa::dec::loads_in_flight(pl.slots) * (32 / (int)(Dp / 8));
+    const int64_t round = fa::dec::WARPS * fa::dec::loads_in_flight(pl.slots) * (32 / (int)(Dp / 8));
     const int64_t max_splits = std::max<int64_t>(1, (nk + 4 * round - 1) / (4 * round));
-    const int64_t want = std::max<int64_t>(1, (8 * (int64_t)sms + BH - 1) / BH);
-    int64_t splits = std::min<int64_t>(want, max_splits);
-    int64_t chunk = (nk + splits - 1) / splits;
-    chunk = (chunk + round - 1) / round * round;
-    splits = (nk + chunk - 1) / chunk;
+    wave = std::max<int64_t>(1, wave);
+    int64_t cand[24];
+    int nc = 0;
+    for (int64_t s = 1; s <= std::min<int64_t>(16, max_splits); ++s) cand[nc++] = s;
+    for (int64_t k = 1; k <= 8; ++k) {
+        const int64_t s = std::min<int64_t>(max_splits, k * wave / BH);
+        if (s > cand[nc - 1]) cand[nc++] = s;  // ascending, no repeats
+    }
+    auto chunk_of = [&](int64_t s) { return ((nk + s - 1) / s + round - 1) / round * round; };
+    double cost[24];
+    double best = 0.0;
+    for (int i = 0; i < nc; ++i) {
+        const int64_t chunk = chunk_of(cand[i]), splits = (nk + chunk - 1) / chunk;
+        const double partials = splits > 1 ? 2.0 * (double)(BH * nq * splits) * (double)(d + 1) * 4.0 : 0.0;
+        cost[i] = (double)((BH * splits + wave - 1) / wave) * (double)chunk * (double)(4 * d) * (double)wave + partials;
+        best = i == 0 ? cost[i] : std::min(best, cost[i]);
+    }
+    int pick = 0;
+    while (cost[pick] > 1.02 * best) ++pick;
+    const int64_t chunk = chunk_of(cand[pick]);
+    const int64_t splits = (nk + chunk - 1) / chunk;
     pl.splits = (int)splits;
     pl.chunk = (int)chunk;
     pl.ws_bytes = splits > 1 ? (size_t)(BH * nq * splits) * (size_t)(d + 1) * sizeof(float) : 0;
@@ -361,6 +386,46 @@ fa_status decode_args(const void* q, const void* k, const void* v, const void* o
     return FA_OK;
 }
 
+// Resident CTAs per SM of the partial kernel instance serving `slots` query
+// rows at head size d (cached per device); 0 if the query fails.
+template <int D, int QM, bool PAD>
+int dec_ctas_per_sm(int dev)
+{
+    static std::atomic<int> cache[MAX_DEVICES];
+    if (dev < 0 || dev >= MAX_DEVICES) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fa::dec::fa_decode_partial_kernel<D, QM, PAD>,
+                                                               fa::dec::THREADS, 0) == cudaSuccess)
+        cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+template <int D, bool PAD>
+int dec_ctas_per_sm_d(int dev, int slots)
+{
+    switch (slots) {
+    case 1: return dec_ctas_per_sm<D, 1, PAD>(dev);
+    case 2: return dec_ctas_per_sm<D, 2, PAD>(dev);
+    case 4: return dec_ctas_per_sm<D, 4, PAD>(dev);
+    default: return dec_ctas_per_sm<D, 8, PAD>(dev);
+    }
+}
+
+// The split plan on this device: one wave is the partial kernel's resident
+// CTAs per SM times the SMs.  FA_ERR_CUDA if the occupancy query fails.
+fa_status device_decode_plan(int dev, const DevInfo& info, int64_t BH, int64_t nq, int64_t nk, int64_t d,
+                             DecodePlan* pl)
+{
+    const int slots = decode_slots(nq);
+    const int per_sm = d == 128 ? dec_ctas_per_sm_d<128, false>(dev, slots)
+                       : d == 64 ? dec_ctas_per_sm_d<64, false>(dev, slots)
+                       : d > 64  ? dec_ctas_per_sm_d<128, true>(dev, slots)
+                                 : dec_ctas_per_sm_d<64, true>(dev, slots);
+    if (per_sm <= 0) return FA_ERR_CUDA;
+    *pl = decode_plan(BH, nq, nk, d, (int64_t)per_sm * info.sms);
+    return FA_OK;
+}
+
 template <int D, int QM, bool PAD>
 fa_status launch_decode(const fa::dec::Params& p, int64_t BH, cudaStream_t st)
 {
@@ -396,7 +461,9 @@ fa_status decode_run(const void* q, const void* k, const void* v, void* o, float
     if (ds != FA_OK) return ds;
     const int64_t BH = B * H;
     const size_t qb = (size_t)(BH * Nq * d * 2), kb = (size_t)(BH * Nk * d * 2), lb = (size_t)(BH * Nq * 4);
-    const DecodePlan pl = decode_plan(BH, Nq, Nk, d, info.sms);
+    DecodePlan pl;
+    const fa_status ps = device_decode_plan(dev, info, BH, Nq, Nk, d, &pl);
+    if (ps != FA_OK) return ps;
     if (pl.ws_bytes > 0) {
         if (!ws || ws_bytes < pl.ws_bytes) return FA_ERR_INVALID_ARG;
         if (overlaps(ws, pl.ws_bytes, o, qb) || overlaps(ws, pl.ws_bytes, lse, lb) || overlaps(ws, pl.ws_bytes, q, qb) ||
@@ -472,8 +539,10 @@ fa_status fa_decode_static(const void* q, const void* k, const void* v, void* o,
     DevInfo info;
     const fa_status ds = sm103_device(&dev, &info);
     if (ds != FA_OK) return ds;
-    const size_t need = decode_plan(B * H, Nq, Nk, d, info.sms).ws_bytes;
-    if (need > FA_DECODE_STATIC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
+    DecodePlan pl;
+    const fa_status ps = device_decode_plan(dev, info, B * H, Nq, Nk, d, &pl);
+    if (ps != FA_OK) return ps;
+    if (pl.ws_bytes > FA_DECODE_STATIC_SCRATCH_BYTES) return FA_ERR_TOO_LARGE;
     void* scratch = static_scratch(dev);
     if (!scratch) return FA_ERR_CUDA;
     return decode_run(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, scratch, FA_DECODE_STATIC_SCRATCH_BYTES,
@@ -490,7 +559,10 @@ fa_status fa_decode_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk
     DevInfo info;
     const fa_status ds = sm103_device(&dev, &info);
     if (ds != FA_OK) return ds;
-    *bytes = decode_plan(B * H, Nq, Nk, d, info.sms).ws_bytes;
+    DecodePlan pl;
+    const fa_status ps = device_decode_plan(dev, info, B * H, Nq, Nk, d, &pl);
+    if (ps != FA_OK) return ps;
+    *bytes = pl.ws_bytes;
     return FA_OK;
 }
 
@@ -756,6 +828,18 @@ fa_status fa_debug_skip_k_tile(int tile)
 {
     if (tile < -1) return FA_ERR_INVALID_ARG;
     g_debug_skip_k.store(tile, std::memory_order_relaxed);
+    return FA_OK;
+}
+
+fa_status fa_debug_decode_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d, int64_t wave, int* splits,
+                               int* chunk)
+{
+    if (!splits || !chunk || wave < 1) return FA_ERR_INVALID_ARG;
+    const fa_status st = decode_check(B, H, Nq, Nk, d, 0);
+    if (st != FA_OK) return st;
+    const DecodePlan pl = decode_plan(B * H, Nq, Nk, d, wave);
+    *splits = pl.splits;
+    *chunk = pl.chunk;
     return FA_OK;
 }
 

@@ -1,6 +1,7 @@
 """The C-ABI library builds, loads and exports what include/fa.h declares, and
 rejects bad arguments before touching the GPU (no compute call is made)."""
 import ctypes
+import itertools
 import os
 import re
 import shutil
@@ -150,14 +151,18 @@ def test_static_decode_checks_arguments_first(lib):
 
 def test_static_decode_argument_errors_come_before_the_size_check(lib):
     """fa_decode_static gives a call that fa_decode would refuse the same
-    status, at sizes whose scratch need exceeds the static array (B*H = 1215
-    heads of 8 query rows: two splits each, about 10 MB of partial results):
-    the scale, alignment and overlap checks run before the device is queried
-    and before FA_ERR_TOO_LARGE is considered."""
+    status, at sizes whose scratch need exceeds the static array (1000 heads
+    of 8 query rows over 4096 keys: at least three splits each, 11.8 MB of
+    partial results or more at any occupancy): the scale, alignment and
+    overlap checks run before the device is queried and before
+    FA_ERR_TOO_LARGE is considered."""
     vp = ctypes.c_void_p
+    for wave in (152, 304, 608, 912, 1216):
+        splits, _ = fa.debug_decode_plan(1000, 1, 8, 4096, 128, wave)
+        assert 1000 * 8 * splits * 129 * 4 > 8 << 20
 
     def call(q=P, o=4 * P, lse=5 * P, scale=0.1):
-        return lib.fa_decode_static(vp(q), vp(2 * P), vp(3 * P), vp(o), vp(lse), 1215, 1, 8, 4096, 128, 0, scale,
+        return lib.fa_decode_static(vp(q), vp(2 * P), vp(3 * P), vp(o), vp(lse), 1000, 1, 8, 4096, 128, 0, scale,
                                     None)
 
     assert call(scale=float("nan")) == 1
@@ -165,6 +170,55 @@ def test_static_decode_argument_errors_come_before_the_size_check(lib):
     assert call(q=P + 8) == 2
     assert call(lse=5 * P + 2) == 2
     assert call(o=3 * P + 16) == 1  # o overlaps v
+
+
+def test_decode_plan_covers_the_keys_in_whole_rounds(lib):
+    """Every split plan cuts the key range into chunks of whole rounds (32
+    keys at the least) that cover it exactly once, each at least 4 rounds
+    long when the range is split."""
+    for BH, Nq, Nk, d, wave in itertools.product((1, 3, 8, 64, 256, 1000, 4096), (1, 2, 4, 8),
+                                                  (1, 100, 1000, 4096, 32768, 100000), (40, 64, 96, 128),
+                                                  (152, 608, 1216)):
+        splits, chunk = fa.debug_decode_plan(BH, 1, Nq, Nk, d, wave)
+        assert (splits - 1) * chunk < Nk <= splits * chunk, (BH, Nq, Nk, d, wave)
+        assert chunk % 32 == 0
+        assert splits == 1 or chunk >= 128
+
+
+def test_decode_plan_fills_whole_waves(lib):
+    """The partial kernel's CTAs take waves of `wave` resident CTAs; a last
+    wave of a few CTAs costs a whole chunk while the rest of the GPU idles.
+    The decode bench workload (B8 H32, one query row, 32768 keys, d = 128; 4
+    CTAs per SM on 152 SMs): 7 chunks a head give 1792 CTAs in 2.95 waves,
+    where 5 chunks would give 1280, two waves and 64 CTAs.  At B2 H32, 19
+    chunks a head give 1216 CTAs, two waves exactly.  Over many head counts,
+    whenever the heads hold two waves of the shortest chunks (4 rounds of 128
+    keys), the CTAs fill at least 90% of the waves they take."""
+    assert fa.debug_decode_plan(8, 32, 1, 32768, 128, 608) == (7, 4736)
+    assert fa.debug_decode_plan(2, 32, 1, 32768, 128, 608) == (19, 1792)
+    for BH, Nk, wave in itertools.product(range(1, 1200, 7), (32768, 65536, 100000), (304, 608, 912, 1216)):
+        if BH * -(-Nk // 512) < 2 * wave:
+            continue
+        splits, _ = fa.debug_decode_plan(BH, 1, 1, Nk, 128, wave)
+        ctas = BH * splits
+        assert ctas / (-(-ctas // wave) * wave) >= 0.9, (BH, Nk, wave, splits)
+
+
+def test_decode_plan_weighs_the_partials(lib):
+    """Splitting 1100 heads of 8 query rows over 1024 keys would shorten the
+    last wave but write and read back more partial results than it saves:
+    the plan keeps one chunk a head."""
+    assert fa.debug_decode_plan(11, 100, 8, 1024, 128, 608) == (1, 1024)
+
+
+def test_decode_plan_argument_checks(lib):
+    with pytest.raises(fa.FaError) as e:
+        fa.debug_decode_plan(1, 1, 1, 64, 128, 0)  # wave < 1
+    assert e.value.code == 1
+    with pytest.raises(fa.FaError) as e:
+        fa.debug_decode_plan(1, 1, 9, 64, 128, 608)  # more query rows than the kernel takes
+    assert e.value.code == 2
+    assert lib.fa_debug_decode_plan(1, 1, 1, 64, 128, 608, None, None) == 1
 
 
 def test_decode_workspace_query_checks_arguments(lib):

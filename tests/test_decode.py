@@ -100,7 +100,8 @@ def test_decode_padding_is_exact():
 
 
 def test_split_and_unsplit_key_ranges():
-    """Many heads (one split each) and one head (many splits) give the oracle."""
+    """Many heads (a few chunks each) and one head (many chunks) give the
+    oracle."""
     for B, H in ((64, 16), (1, 1)):
         q, k, v = rand(B, H, 1, 6000, 128, seed=B * 7 + H)
         o, lse, nbytes = run_guarded(q.cuda(), k.cuda(), v.cuda(), False, 0.088)
