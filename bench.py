@@ -77,18 +77,18 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "b96eba35e10a5909bcccebb5dc216890e0fe98ec6a361449d2a7036502776cde",
-        "bytes": 4 * (201_461_248 + 45_022_976),
+        "sha256": "63c89fd2424941a0b2e2b4276808a33cccb52e34a5c8e1a32cf2a2c991a53581",
+        "bytes": 4 * (201_463_552 + 45_208_576),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
-        "sha256": "90da0681e1e8cee8c28f6acd623701cc96187b86c16a1f6281d00d5b8bc8d646",
-        "bytes": 4 * (406_646_016 + 217_909_760),
+        "sha256": "4d360fedaed9e0ee3daead10b5c33a2471d2d1898f8368ef4d8adcea5c3b0cdb",
+        "bytes": 4 * (406_228_224 + 218_755_328),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "b63cd7396eebb754f8525ef3730603a73fe834ddcd7860e19028c9f0eff142f2",
-        "bytes": 285_238_784 + 210_507_008,
+        "sha256": "cf5226a627ed20cc1ec1cb0e1bb49076fda69a8469752bb75853a16db3e20681",
+        "bytes": 285_283_328 + 210_664_960,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
