@@ -705,7 +705,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 
     // 1. D, L * log2 e, zeroed dQ accumulator.
     const int64_t rows = BH * sh.Np;
-    fa::bwd::fa_bwd_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(
+    fa::bwd::fa_bwd_prep_kernel<<<(unsigned)((rows + 8 * fa::bwd::PREP_ROWS - 1) / (8 * fa::bwd::PREP_ROWS)), 256, 0,
+                                   st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, dsum, acc,
         (int)N, (int)sh.Np, (int)d, (int)sh.Dp, rows);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;

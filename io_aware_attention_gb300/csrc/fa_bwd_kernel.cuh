@@ -619,42 +619,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // D_i = dO_i . O_i and L_i * log2 e for every row i < Np of every head (rows
 // >= N: D = 0, L * log2 e = +inf, so their recomputed P is 0), and the fp32
-// dQ accumulator (Dp floats a row) zeroed.  One warp per row; a lane takes 8
-// consecutive elements (d is a multiple of 8, at most 256 per pass).
-__global__ void __launch_bounds__(256)
+// dQ accumulator (Dp floats a row) zeroed.  A warp takes PREP_ROWS
+// consecutive rows (one head's: Np is a multiple of 64) and issues all their
+// loads before it reduces any, so that enough bytes are in flight; lane l
+// takes elements 8l .. 8l + 7 of a row (d <= 128).
+constexpr int PREP_ROWS = 4;
+
+__global__ void __launch_bounds__(256, 4)
     fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ lse2, float* __restrict__ dsum,
                        float* __restrict__ dq_acc, int N, int Np, int d, int Dp, int64_t rows)
 {
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t row0 = ((int64_t)blockIdx.x * 8 + (threadIdx.x >> 5)) * PREP_ROWS;
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
-    const int64_t bh = row / Np;
-    const int i = (int)(row - bh * Np);
-    float acc = 0.f;
-    if (i < N) {
-        const int64_t base = (bh * N + i) * d;
-        for (int c = lane * 8; c < d; c += 256) {
-            const uint4 a = *reinterpret_cast<const uint4*>(o + base + c);
-            const uint4 b = *reinterpret_cast<const uint4*>(dout + base + c);
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    if (row0 >= rows) return;
+    const int64_t bh = row0 / Np;
+    const int i0 = (int)(row0 - bh * Np);
+    const int c = lane * 8;
+    const __nv_bfloat16* const po = o + (bh * N + i0) * d + c;
+    const __nv_bfloat16* const pd = dout + (bh * N + i0) * d + c;
+    uint4 a[PREP_ROWS], b[PREP_ROWS];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[j]));
-                const float2 bf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[j]));
-                acc = fmaf(af.x, bf.x, acc);
-                acc = fmaf(af.y, bf.y, acc);
-            }
+    for (int r = 0; r < PREP_ROWS; ++r) {
+        a[r] = b[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (i0 + r < N && c < d) {
+            a[r] = *reinterpret_cast<const uint4*>(po + r * d);
+            b[r] = *reinterpret_cast<const uint4*>(pd + r * d);
         }
     }
+    float acc[PREP_ROWS];
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-    if (lane == 0) {
-        dsum[row] = i < N ? acc : 0.f;
-        lse2[row] = i < N ? lse[bh * N + i] * 1.4426950408889634074f : __int_as_float(0x7f800000);
+    for (int r = 0; r < PREP_ROWS; ++r) {
+        const uint32_t aw[4] = {a[r].x, a[r].y, a[r].z, a[r].w}, bw[4] = {b[r].x, b[r].y, b[r].z, b[r].w};
+        acc[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 af = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[j]));
+            const float2 bf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[j]));
+            acc[r] = fmaf(af.x, bf.x, acc[r]);
+            acc[r] = fmaf(af.y, bf.y, acc[r]);
+        }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], m);
     }
-    float4* const z = reinterpret_cast<float4*>(dq_acc + row * Dp);
-    for (int c = lane; c < Dp / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < PREP_ROWS) {
+        float v = acc[0];
+#pragma unroll
+        for (int r = 1; r < PREP_ROWS; ++r)
+            if (lane == r) v = acc[r];
+        const int i = i0 + lane;
+        dsum[row0 + lane] = i < N ? v : 0.f;
+        lse2[row0 + lane] = i < N ? lse[bh * N + i] * 1.4426950408889634074f : __int_as_float(0x7f800000);
+    }
+    // The warp's rows are consecutive: one block of PREP_ROWS * Dp floats.
+    float4* const z = reinterpret_cast<float4*>(dq_acc + row0 * Dp);
+    for (int k = lane; k < PREP_ROWS * Dp / 4; k += 32) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // dQ = bf16(scale * accumulator) for rows < N; the accumulator is
