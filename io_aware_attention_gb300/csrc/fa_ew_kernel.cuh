@@ -117,14 +117,13 @@ __global__ void __launch_bounds__(THREADS, 4) fa_bias_gelu_dropout_kernel(const 
     __syncthreads();
     const int64_t per_round = (int64_t)gridDim.x * THREADS * UNROLL;
     for (int64_t v0 = (int64_t)blockIdx.x * THREADS * UNROLL + threadIdx.x; v0 < p.n8; v0 += per_round) {
-        uint4 xv[UNROLL], bv[UNROLL];
+        uint4 xv[UNROLL];
         uint32_t kb[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t v = v0 + (int64_t)u * THREADS;
             if (v < p.n8) {
                 xv[u] = ld_stream(p.x + v * 8);
-                bv[u] = __ldg(reinterpret_cast<const uint4*>(p.bias) + col8_of<WIDE>(v, p));
                 kb[u] = p.keep ? (uint32_t)__ldg(p.keep + v) : 0xFFu;
             }
         }
@@ -132,10 +131,13 @@ __global__ void __launch_bounds__(THREADS, 4) fa_bias_gelu_dropout_kernel(const 
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t v = v0 + (int64_t)u * THREADS;
             if (v < p.n8) {
-                const uint32_t w0 = chain2(xv[u].x, bv[u].x, ftab[kb[u] & 3u]);
-                const uint32_t w1 = chain2(xv[u].y, bv[u].y, ftab[(kb[u] >> 2) & 3u]);
-                const uint32_t w2 = chain2(xv[u].z, bv[u].z, ftab[(kb[u] >> 4) & 3u]);
-                const uint32_t w3 = chain2(xv[u].w, bv[u].w, ftab[(kb[u] >> 6) & 3u]);
+                // The bias (L1/L2-resident) is loaded here, so that its registers
+                // hold no vector in flight.
+                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.bias) + col8_of<WIDE>(v, p));
+                const uint32_t w0 = chain2(xv[u].x, bv.x, ftab[kb[u] & 3u]);
+                const uint32_t w1 = chain2(xv[u].y, bv.y, ftab[(kb[u] >> 2) & 3u]);
+                const uint32_t w2 = chain2(xv[u].z, bv.z, ftab[(kb[u] >> 4) & 3u]);
+                const uint32_t w3 = chain2(xv[u].w, bv.w, ftab[(kb[u] >> 6) & 3u]);
                 // Streaming store: y is not read again by this kernel.
                 asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p.y + v * 8), "r"(w0), "r"(w1),
                              "r"(w2), "r"(w3)
