@@ -77,8 +77,8 @@ EW_SOURCES = ("fa_ew_kernel.cuh", "ptx.cuh", "fa_api.cu")
 MEASURED_TRAFFIC = {
     ("b8_h32_n4096_d128_causal", "fwd"): {
         "sources": FWD_SOURCES,
-        "sha256": "63c89fd2424941a0b2e2b4276808a33cccb52e34a5c8e1a32cf2a2c991a53581",
-        "bytes": 4 * (201_463_552 + 45_208_576),
+        "sha256": "71c822ee1441c996e8c74e94626390f0491be3ee090d4363e3ec00823ce04fa0",
+        "bytes": 4 * (201_403_136 + 45_192_448),
         "captured_on": "B=2, H=32, N=4096, d=128, causal; x4"},
     ("b8_h32_n4096_d128_causal", "bwd"): {
         "sources": BWD_SOURCES,
@@ -87,8 +87,8 @@ MEASURED_TRAFFIC = {
         "captured_on": "B=2, H=32, N=4096, d=128, causal; main kernel only; x4"},
     ("ew_b8_t4096_d4096_p0.1", "ew"): {
         "sources": EW_SOURCES,
-        "sha256": "cf5226a627ed20cc1ec1cb0e1bb49076fda69a8469752bb75853a16db3e20681",
-        "bytes": 285_283_328 + 210_664_960,
+        "sha256": "a1280852145bf2c19457b9232e3cdebf52f538b2b2dcaad13f9d284a96159670",
+        "bytes": 285_297_664 + 210_903_040,
         "captured_on": "the full workload (537 MB on the device)"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
