@@ -204,6 +204,30 @@ def test_decode_plan_fills_whole_waves(lib):
         assert ctas / (-(-ctas // wave) * wave) >= 0.9, (BH, Nk, wave, splits)
 
 
+def test_decode_plan_search_matches_every_split_count(lib):
+    """The plan tries a few dozen split counts, not all of them: up to 16,
+    and the fullest for 1 to 8 waves.  Against a search over every count
+    from 1 to the most the 4-round minimum allows, under the plan's own cost
+    (waves x chunk x K and V bytes a key x wave, plus the partial results
+    written and read back), the chosen count is within 5% of the best.  The
+    counts it does not try are many waves of the shortest chunks; the cost
+    does not charge a CTA's fixed start-up and merge work, which those pay
+    most.  One query row at d = 128: rounds of 128 keys."""
+    rnd, d, nq = 128, 128, 1
+
+    def cost(BH, Nk, wave, s):
+        chunk = (-(-Nk // s) + rnd - 1) // rnd * rnd
+        splits = -(-Nk // chunk)
+        partials = 2.0 * BH * nq * splits * (d + 1) * 4 if splits > 1 else 0.0
+        return -(-(BH * splits) // wave) * chunk * 4 * d * wave + partials
+
+    for BH, Nk, wave in itertools.product((1, 3, 8, 31, 64, 100, 256, 301, 777, 1024, 4096), (4096, 32768, 100000),
+                                          (152, 456, 608, 1216)):
+        splits, chunk = fa.debug_decode_plan(BH, 1, nq, Nk, d, wave)
+        best = min(cost(BH, Nk, wave, s) for s in range(1, -(-Nk // (4 * rnd)) + 1))
+        assert cost(BH, Nk, wave, splits) <= 1.05 * best, (BH, Nk, wave, splits)
+
+
 def test_decode_plan_weighs_the_partials(lib):
     """Splitting 1100 heads of 8 query rows over 1024 keys would shorten the
     last wave but write and read back more partial results than it saves:
